@@ -1,0 +1,171 @@
+/*
+ * CPU oracle for the groupwise int4/int5 weight-only dequant-GEMM.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package entry point's smoke
+ * check and the benchmark's CPU-baseline leg may load or call this code.  It
+ * shares nothing with the CUDA library (no headers, no helpers, no tables):
+ * its code unpacking, its fp16/bf16 decoding and its arithmetic are written
+ * here from the definition and nowhere else.
+ *
+ * What it computes is the plain definition, in fp64, single-threaded:
+ *
+ *     Y[t][n] = sum_k  x[t][k] * ( s[n][k/64] * q[n][k] ),   k ascending
+ *     A[t][n] = sum_k |x[t][k] * ( s[n][k/64] * q[n][k] )|
+ *
+ * - groupwise-int weights with one scale per 64 K-columns per row
+ *   ("ninfer-3080 docs/performance.md", the cuBLAS prefill route section:
+ *   cuBLAS reduces over all of K and so cannot apply a scale per 64 columns);
+ * - the Q4 and Q5 codecs, Q5 carrying one more (high) bit per code
+ *   (same page, the small-T kernels section on the Q5 counterpart);
+ * - an fp64 oracle as the accuracy yardstick (same page, the A8 prefill
+ *   routes section, which reports relative L2 against an FP64 oracle);
+ * - codes are symmetric two's complement with no zero point: int4 in [-8, 7],
+ *   int5 in [-16, 15]; scales are IEEE fp16; activations are bf16.
+ *
+ * Every product x * s * q is exact in fp64 (bf16 has 8 significant bits,
+ * fp16 11, a code at most 5), so the only roundings are those of the running
+ * sum, in ascending k.
+ *
+ * Canonical packing read here (the library's input format):
+ * - int4: ceil(K/2) bytes per row; byte j holds code 2j in bits 0-3 and code
+ *   2j+1 in bits 4-7.
+ * - int5: ceil(5K/8) bytes per row; LSB-first bitstream, code k in bits
+ *   5k .. 5k+4.
+ * Scales: fp16 bit patterns, row-major [N][ceil(K/64)]; the last group of a
+ * row may be shorter than 64 when K is not a multiple of 64 (the library
+ * itself requires K % 64 == 0; the oracle accepts any K so that tiny
+ * brute-force cases can run).
+ * X: bf16 bit patterns, row-major [T][K].  Y, A: fp64, row-major [T][N].
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_GROUP 64
+
+/* IEEE binary16 -> double, from the field definitions. */
+static double oracle_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int mant = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)mant, -24);                 /* subnormal: m * 2^-24 */
+    else if (expo == 31)
+        v = mant ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + mant), expo - 25);  /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double: a bf16 pattern is the top half of an IEEE binary32. */
+static double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int qgemm_oracle_row_bytes(int bits, int K)
+{
+    if ((bits != 4 && bits != 5) || K < 0)
+        return -1;
+    return (int)(((long)K * bits + 7) / 8);
+}
+
+int qgemm_oracle_groups(int K)
+{
+    return (K + ORACLE_GROUP - 1) / ORACLE_GROUP;
+}
+
+/* Two's-complement code k of one canonical row. */
+static int oracle_code(int bits, const uint8_t *row, int k)
+{
+    if (bits == 4) {
+        int byte = row[k >> 1];
+        int nib = (k & 1) ? (byte >> 4) : (byte & 0x0f);
+        return nib >= 8 ? nib - 16 : nib;
+    } else {
+        long bit = 5L * k;
+        int v = 0;
+        for (int b = 0; b < 5; ++b) {
+            long p = bit + b;
+            v |= ((row[p >> 3] >> (p & 7)) & 1) << b;
+        }
+        return v >= 16 ? v - 32 : v;
+    }
+}
+
+/* Integer codes [N][K] (unpacking only). */
+int qgemm_oracle_unpack(int bits, int N, int K, const uint8_t *packed, int8_t *codes)
+{
+    int rb = qgemm_oracle_row_bytes(bits, K);
+    if (rb < 0 || N < 0 || ((N > 0 && K > 0) && (!packed || !codes)))
+        return -1;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            codes[(size_t)n * K + k] = (int8_t)oracle_code(bits, packed + (size_t)n * rb, k);
+    return 0;
+}
+
+/* Dequantised weights W[n][k] = s[n][k/64] * q[n][k], fp64 [N][K]. */
+int qgemm_oracle_dequant(int bits, int N, int K, const uint8_t *packed,
+                         const uint16_t *scales, double *W)
+{
+    int rb = qgemm_oracle_row_bytes(bits, K);
+    int G = qgemm_oracle_groups(K);
+    if (rb < 0 || N < 0)
+        return -1;
+    for (int n = 0; n < N; ++n) {
+        const uint8_t *row = packed + (size_t)n * rb;
+        for (int k = 0; k < K; ++k) {
+            double s = oracle_half_to_double(scales[(size_t)n * G + k / ORACLE_GROUP]);
+            W[(size_t)n * K + k] = s * (double)oracle_code(bits, row, k);
+        }
+    }
+    return 0;
+}
+
+/*
+ * Y[t][n] and A[t][n] as defined in the header comment.  Row n is dequantised
+ * once into a scratch row, then dotted with every activation column in
+ * ascending k.  Returns 0, or -1 on bad arguments or allocation failure.
+ */
+int qgemm_oracle_gemm(int bits, int N, int K, int T, const uint8_t *packed,
+                      const uint16_t *scales, const uint16_t *X, double *Y, double *A)
+{
+    int rb = qgemm_oracle_row_bytes(bits, K);
+    int G = qgemm_oracle_groups(K);
+    if (rb < 0 || N < 0 || T < 0)
+        return -1;
+    if (N == 0 || T == 0)
+        return 0;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    if (!w)
+        return -1;
+    for (int n = 0; n < N; ++n) {
+        const uint8_t *row = packed + (size_t)n * rb;
+        for (int k = 0; k < K; ++k) {
+            double s = oracle_half_to_double(scales[(size_t)n * G + k / ORACLE_GROUP]);
+            w[k] = s * (double)oracle_code(bits, row, k);
+        }
+        for (int t = 0; t < T; ++t) {
+            const uint16_t *xr = X + (size_t)t * K;
+            double acc = 0.0, mag = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double p = oracle_bf16_to_double(xr[k]) * w[k];
+                acc += p;
+                mag += fabs(p);
+            }
+            Y[(size_t)t * N + n] = acc;
+            if (A)
+                A[(size_t)t * N + n] = mag;
+        }
+    }
+    free(w);
+    return 0;
+}

@@ -1,0 +1,268 @@
+"""Pins of the CPU oracle to facts it does not compute itself.
+
+The oracle (oracle/qgemm_oracle.c) is the fp64 definition of the groupwise
+dequant-GEMM.  These tests check it against:
+
+* hand-worked cases whose values were derived on paper (tests/golden/);
+* exact rational arithmetic (Python integers/Fractions) from the codes as drawn,
+  before packing, with numpy's own fp16/bf16 decoding -- the oracle's fp64
+  result must lie within the recursive-summation error bound of the exact sum;
+* brute force over every int4 byte and every int5 code at every bit offset,
+  with the expected codes built by integer arithmetic in the test;
+* numpy's float64 matmul on weights dequantised by the test;
+* invariants the definition implies: linearity over disjoint supports,
+  identity and permutation weights, power-of-two scaling, negated scales,
+  int5 restricted to [-8, 7] equal to int4, column independence.
+
+Each pin is a function of the loaded library so that ``test_planted_mistakes``
+can re-run the whole set against copies of the oracle with one mistake
+planted (a dropped term, a wrong sign extension, swapped nibbles, transposed
+scales, ...) and confirm that some pin fails for every one of them.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_only_groupwise_gb300 import synth
+from tests import golden_io
+
+U = 2.0 ** -53
+
+
+# ------------------------------------------------------------ independent decoding
+
+def fp16_values(bits: np.ndarray) -> np.ndarray:
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def exact_gemm(codes, scales_bits, x_bits):
+    """Exact Y and A as Fractions, from unpacked integer codes."""
+    N, K = codes.shape
+    T = x_bits.shape[0]
+    s = fp16_values(scales_bits)
+    x = bf16_values(x_bits)
+    Y = [[None] * N for _ in range(T)]
+    A = [[None] * N for _ in range(T)]
+    for t in range(T):
+        for n in range(N):
+            acc = Fraction(0)
+            mag = Fraction(0)
+            for k in range(K):
+                p = Fraction(float(x[t, k])) * Fraction(float(s[n, k // 64])) * int(codes[n, k])
+                acc += p
+                mag += abs(p)
+            Y[t][n] = acc
+            A[t][n] = mag
+    return Y, A
+
+
+def small_case(seed, N, K, T, bits):
+    w = synth.weights(seed, N, K, bits)
+    x = synth.activations(seed, T, K, outliers=True)
+    return w, x
+
+
+# ------------------------------------------------------------ the pins
+
+def pin_golden(lib):
+    for fname in ("int4_hand.txt", "int5_hand.txt"):
+        for name, c in golden_io.load(fname).items():
+            Y, A = oracle.gemm(c["bits"], c["packed"], c["scales"], c["x"], c["N"], c["K"], lib=lib)
+            assert np.array_equal(Y, c["y"]), (fname, name, Y, c["y"])
+            assert np.array_equal(A, c["a"]), (fname, name, A, c["a"])
+
+
+def pin_exact_rational(lib):
+    shapes = [(1, 2, 1, 4), (3, 8, 2, 5), (5, 64, 3, 4), (4, 100, 2, 5), (7, 128, 4, 4), (2, 192, 3, 5)]
+    for seed, (N, K, T, bits) in enumerate(shapes):
+        w, x = small_case(seed + 11, N, K, T, bits)
+        Y, A = oracle.gemm(bits, w["packed"], w["scales"], x, N, K, lib=lib)
+        Ye, Ae = exact_gemm(w["codes"], w["scales"], x)
+        for t in range(T):
+            for n in range(N):
+                bound = K * U * float(Ae[t][n])
+                assert abs(Fraction(float(Y[t, n])) - Ye[t][n]) <= Fraction(bound), (N, K, T, bits, t, n)
+                assert abs(Fraction(float(A[t, n])) - Ae[t][n]) <= Fraction(bound), (N, K, T, bits, t, n)
+
+
+def pin_bruteforce_int4(lib):
+    # row b holds the single byte b: codes (low nibble, high nibble)
+    packed = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    scales = np.full((256, 1), 0x3C00, np.uint16)
+    x = np.array([[0x3F80, 0], [0, 0x3F80]], np.uint16)           # e_0, e_1
+    Y, _ = oracle.gemm(4, packed, scales, x, 256, 2, lib=lib)
+    b = np.arange(256, dtype=np.int32)
+    lo = ((b << 4).astype(np.uint8).view(np.int8) >> 4).astype(np.float64)   # arithmetic shift
+    hi = (b.astype(np.uint8).view(np.int8) >> 4).astype(np.float64)
+    assert np.array_equal(Y[0], lo)
+    assert np.array_equal(Y[1], hi)
+    assert np.array_equal(oracle.unpack(4, packed, 256, 2, lib=lib).astype(np.float64), np.stack([lo, hi], 1))
+
+
+def pin_bruteforce_int5(lib):
+    # K = 8 codes per row (40 bits); row (p, v) holds value v at position p, zeros elsewhere
+    rows, want = [], []
+    for p in range(8):
+        for v in range(-16, 16):
+            stream = (v & 31) << (5 * p)
+            rows.append(list(stream.to_bytes(5, "little")))
+            want.append((p, v))
+    packed = np.array(rows, np.uint8)
+    N = packed.shape[0]
+    codes = oracle.unpack(5, packed, N, 8, lib=lib)
+    for r, (p, v) in enumerate(want):
+        exp = np.zeros(8, np.int8)
+        exp[p] = v
+        assert np.array_equal(codes[r], exp), (p, v, codes[r])
+    scales = np.full((N, 1), 0x3C00, np.uint16)
+    x = np.eye(8, dtype=np.uint16) * np.uint16(0x3F80)
+    Y, _ = oracle.gemm(5, packed, scales, x, N, 8, lib=lib)
+    for r, (p, v) in enumerate(want):
+        col = np.zeros(8)
+        col[p] = v
+        assert np.array_equal(Y[:, r], col)
+
+
+def pin_numpy_matmul(lib):
+    for seed, (N, K, T, bits) in enumerate([(33, 256, 5, 4), (17, 320, 3, 5), (64, 512, 2, 4)]):
+        w, x = small_case(seed + 101, N, K, T, bits)
+        W = w["codes"].astype(np.float64) * np.repeat(fp16_values(w["scales"]), 64, axis=1)[:, :K]
+        Xd = bf16_values(x)
+        ref = Xd @ W.T
+        mag = np.abs(Xd) @ np.abs(W).T
+        Y, A = oracle.gemm(bits, w["packed"], w["scales"], x, N, K, lib=lib)
+        assert np.all(np.abs(Y - ref) <= 2 * K * U * mag), (N, K, T, bits)
+        assert np.all(np.abs(A - mag) <= 2 * K * U * mag)
+        Wo = oracle.dequant(bits, w["packed"], w["scales"], N, K, lib=lib)
+        assert np.array_equal(Wo, W)
+
+
+def pin_linearity_exact(lib):
+    # integer-valued data: every partial sum is exact, so equalities are bitwise
+    rng = np.random.default_rng(5)
+    N, K, T = 9, 128, 3
+    codes = rng.integers(-8, 8, size=(N, K))
+    packed = synth.pack_canonical(codes, 4)
+    scales = synth.fp64_to_fp16_bits(2.0 ** rng.integers(-2, 3, size=(N, 2)).astype(np.float64))
+    xv = rng.integers(-4, 5, size=(T, K)).astype(np.float64)
+    x = synth.fp64_to_bf16_bits(xv)
+    even = np.zeros_like(xv)
+    even[:, 0::2] = xv[:, 0::2]
+    odd = xv - even
+    Y, _ = oracle.gemm(4, packed, scales, x, N, K, lib=lib)
+    Y1, _ = oracle.gemm(4, packed, scales, synth.fp64_to_bf16_bits(even), N, K, lib=lib)
+    Y2, _ = oracle.gemm(4, packed, scales, synth.fp64_to_bf16_bits(odd), N, K, lib=lib)
+    assert np.array_equal(Y, Y1 + Y2)
+    Y3, _ = oracle.gemm(4, packed, scales, synth.fp64_to_bf16_bits(xv * 8.0), N, K, lib=lib)
+    assert np.array_equal(Y3, 8.0 * Y)
+
+
+def pin_identity_and_permutation(lib):
+    N = K = 64
+    T = 4
+    x = synth.activations(3, T, K, outliers=True)
+    xv = bf16_values(x)
+    eye = np.eye(N, K, dtype=np.int8)
+    ones = np.full((N, 1), 0x3C00, np.uint16)
+    Y, _ = oracle.gemm(4, synth.pack_canonical(eye, 4), ones, x, N, K, lib=lib)
+    assert np.array_equal(Y, xv[:, :N])
+    perm = np.random.default_rng(9).permutation(K)[:N]
+    P = np.zeros((N, K), np.int8)
+    P[np.arange(N), perm] = 1
+    for bits in (4, 5):
+        Y, _ = oracle.gemm(bits, synth.pack_canonical(P, bits), ones, x, N, K, lib=lib)
+        assert np.array_equal(Y, xv[:, perm])
+
+
+def pin_scaling_and_negation(lib):
+    N, K, T = 12, 192, 3
+    w, x = small_case(21, N, K, T, 4)
+    Y, _ = oracle.gemm(4, w["packed"], w["scales"], x, N, K, lib=lib)
+    s2 = w["scales"].copy()
+    s2[5] = synth.fp64_to_fp16_bits(fp16_values(s2[5]) * 4.0)        # row 5 scaled by 2^2
+    Y2, _ = oracle.gemm(4, w["packed"], s2, x, N, K, lib=lib)
+    exp = Y.copy()
+    exp[:, 5] *= 4.0
+    assert np.array_equal(Y2, exp)
+    sneg = w["scales"] ^ np.uint16(0x8000)                           # flip every scale's sign
+    Yn, _ = oracle.gemm(4, w["packed"], sneg, x, N, K, lib=lib)
+    assert np.array_equal(Yn, -Y)
+
+
+def pin_int5_contains_int4(lib):
+    N, K, T = 10, 128, 2
+    codes = synth.uniform_codes(4, 1, N, K, 4)
+    scales = synth.group_scales(4, 2, N, K)
+    x = synth.activations(4, T, K, outliers=False)
+    Y4, _ = oracle.gemm(4, synth.pack_canonical(codes, 4), scales, x, N, K, lib=lib)
+    Y5, _ = oracle.gemm(5, synth.pack_canonical(codes, 5), scales, x, N, K, lib=lib)
+    assert np.array_equal(Y4, Y5)
+
+
+def pin_column_independence(lib):
+    N, K, T = 8, 128, 5
+    w, x = small_case(31, N, K, T, 5)
+    Y, _ = oracle.gemm(5, w["packed"], w["scales"], x, N, K, lib=lib)
+    for t in range(T):
+        Yt, _ = oracle.gemm(5, w["packed"], w["scales"], x[t:t + 1], N, K, lib=lib)
+        assert np.array_equal(Yt[0], Y[t])
+
+
+PINS = [pin_golden, pin_exact_rational, pin_bruteforce_int4, pin_bruteforce_int5, pin_numpy_matmul,
+        pin_linearity_exact, pin_identity_and_permutation, pin_scaling_and_negation,
+        pin_int5_contains_int4, pin_column_independence]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(oracle.load())
+
+
+# ------------------------------------------------------------ planted mistakes
+
+MUTANTS = {
+    "dropped_last_term": ("for (int k = 0; k < K; ++k) {\n                double p",
+                          "for (int k = 0; k < K - 1; ++k) {\n                double p"),
+    "sign_extension": ("return nib >= 8 ? nib - 16 : nib;", "return nib > 8 ? nib - 16 : nib;"),
+    "nibble_order": ("(k & 1) ? (byte >> 4) : (byte & 0x0f)", "(k & 1) ? (byte & 0x0f) : (byte >> 4)"),
+    "transposed_scales": ("w[k] = s * (double)oracle_code(bits, row, k);",
+                          "w[k] = oracle_half_to_double(scales[(size_t)(k / ORACLE_GROUP) * N + n])"
+                          " * (double)oracle_code(bits, row, k); (void)s;"),
+    "int5_sign": ("return v >= 16 ? v - 32 : v;", "return v >= 16 ? v - 31 : v;"),
+    "int5_bit_order": ("& 1) << b;", "& 1) << (4 - b);"),
+    "abs_sum": ("mag += fabs(p);", "mag += p;"),
+    "x_stride": ("const uint16_t *xr = X + (size_t)t * K;", "const uint16_t *xr = X + (size_t)t;"),
+    "half_bias": ("expo - 25);", "expo - 24);"),
+    "half_subnormal": ("ldexp((double)mant, -24);", "ldexp((double)mant, -25);"),
+    "group_width": ("#define ORACLE_GROUP 64", "#define ORACLE_GROUP 128"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new)
+    cpath = tmp_path / "mutant.c"
+    cpath.write_text(mutated)
+    so = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", so, str(cpath), "-lm"], check=True)
+    lib = oracle.load(so)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"

@@ -1,1 +1,245 @@
-"""Groupwise int4/int5 weight-only dequant-GEMM for GB300 (sm_103a)."""
+"""Groupwise int4/int5 weight-only dequant-GEMM for GB300 (sm_103a).
+
+Python binding of the C-ABI library ``_lib/libqgemm.so`` (declared in
+``include/qgemm.h``).  Every function here has the name of the C entry point
+it calls and does argument marshalling only: device pointers and streams are
+taken from torch tensors and streams (or passed as plain integers), and the
+status code is returned as the C function returns it.  All computation runs
+in the library's CUDA kernels; there is no fallback: if the library is
+missing the first call raises.
+
+``GroupwiseWeights`` is a convenience holder that allocates the packed
+buffer and the workspace with torch and binds them to a plan.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libqgemm.so")
+
+QGEMM_OK = 0
+QGEMM_ERR_INVALID_ARG = 1
+QGEMM_ERR_SHAPE = 2
+QGEMM_ERR_ALIGNMENT = 3
+QGEMM_ERR_T_OUT_OF_DOMAIN = 4
+QGEMM_ERR_WORKSPACE = 5
+QGEMM_ERR_CUDA = 6
+QGEMM_ERR_TIMEOUT = 7
+QGEMM_ERR_UNSUPPORTED = 8
+
+QGEMM_INT4 = 4
+QGEMM_INT5 = 5
+
+# every symbol include/qgemm.h declares
+EXPORTS = [
+    "qgemm_status_string", "qgemm_packed_bytes", "qgemm_pack_weights", "qgemm_plan",
+    "qgemm_plan_workspace_bytes", "qgemm_plan_bind", "qgemm_run", "qgemm_run_multi",
+    "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
+    "qgemm_device_status",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QgemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {qgemm_status_string(status)} ({status})" if what else qgemm_status_string(status))
+
+
+def _declare(lib):
+    c = ctypes
+    vp, i32, sz, u64 = c.c_void_p, c.c_int, c.c_size_t, c.c_uint64
+    sig = {
+        "qgemm_status_string": ([i32], c.c_char_p),
+        "qgemm_packed_bytes": ([i32, i32, i32], sz),
+        "qgemm_pack_weights": ([i32, i32, i32, vp, vp, vp, vp], i32),
+        "qgemm_plan": ([i32, i32, i32, i32, c.POINTER(vp)], i32),
+        "qgemm_plan_workspace_bytes": ([vp], sz),
+        "qgemm_plan_bind": ([vp, vp, vp, sz], i32),
+        "qgemm_run": ([vp, vp, i32, vp, vp], i32),
+        "qgemm_run_multi": ([c.POINTER(vp), i32, vp, i32, c.POINTER(vp), vp], i32),
+        "qgemm_plan_destroy": ([vp], i32),
+        "qgemm_plan_route": ([vp, i32], i32),
+        "qgemm_route_name": ([i32], c.c_char_p),
+        "qgemm_launch_count": ([], u64),
+        "qgemm_device_status": ([vp, i32], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+def load(path: str | None = None):
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"qgemm CUDA library not found at {p}; build it with "
+                    "`python -m bit_weight_only_groupwise_gb300.build` (no CPU fallback exists)")
+            lib = _declare(ctypes.CDLL(p))
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+# ------------------------------------------------------------ C entry points
+
+def qgemm_status_string(status: int) -> str:
+    return load().qgemm_status_string(status).decode()
+
+
+def qgemm_packed_bytes(N: int, K: int, codec: int) -> int:
+    return load().qgemm_packed_bytes(N, K, codec)
+
+
+def qgemm_pack_weights(codec, N, K, codes_canonical_dev, scales_fp16_dev, packed_dev, stream=None) -> int:
+    return load().qgemm_pack_weights(codec, N, K, _ptr(codes_canonical_dev), _ptr(scales_fp16_dev),
+                                     _ptr(packed_dev), _stream(stream))
+
+
+def qgemm_plan(N: int, K: int, codec: int, T_max: int):
+    """(status, plan handle)."""
+    h = ctypes.c_void_p()
+    st = load().qgemm_plan(N, K, codec, T_max, ctypes.byref(h))
+    return st, h.value
+
+
+def qgemm_plan_workspace_bytes(plan) -> int:
+    return load().qgemm_plan_workspace_bytes(plan)
+
+
+def qgemm_plan_bind(plan, packed_dev, workspace_dev, ws_bytes: int) -> int:
+    return load().qgemm_plan_bind(plan, _ptr(packed_dev), _ptr(workspace_dev), ws_bytes)
+
+
+def qgemm_run(plan, X, T: int, Y, stream=None) -> int:
+    return load().qgemm_run(plan, _ptr(X), T, _ptr(Y), _stream(stream))
+
+
+def qgemm_run_multi(plans, X, T: int, Ys, stream=None) -> int:
+    n = len(plans)
+    parr = (ctypes.c_void_p * max(n, 1))(*plans)
+    yarr = (ctypes.c_void_p * max(len(Ys), 1))(*[_ptr(y) for y in Ys])
+    return load().qgemm_run_multi(parr, n, _ptr(X), T, yarr, _stream(stream))
+
+
+def qgemm_plan_destroy(plan) -> int:
+    return load().qgemm_plan_destroy(plan)
+
+
+def qgemm_plan_route(plan, T: int) -> int:
+    return load().qgemm_plan_route(plan, T)
+
+
+def qgemm_route_name(route: int) -> str:
+    return load().qgemm_route_name(route).decode()
+
+
+def qgemm_launch_count() -> int:
+    return load().qgemm_launch_count()
+
+
+def qgemm_device_status(stream=None, clear: bool = False) -> int:
+    return load().qgemm_device_status(_stream(stream), 1 if clear else 0)
+
+
+def check(status: int, what: str = "") -> None:
+    if status != QGEMM_OK:
+        raise QgemmError(status, what)
+
+
+# ------------------------------------------------------------ convenience holder
+
+class GroupwiseWeights:
+    """One packed weight matrix bound to a plan (device memory from torch).
+
+    ``codes_canonical`` and ``scales_fp16`` are the canonical packed codes
+    (uint8 [N, row_bytes]) and fp16 bit patterns (uint16/int16 [N, K/64]), as
+    numpy arrays or torch tensors on the host or the device.
+    """
+
+    def __init__(self, codec: int, N: int, K: int, codes_canonical, scales_fp16, T_max: int,
+                 device="cuda", stream=None):
+        import numpy as np
+        import torch
+        self.codec, self.N, self.K, self.T_max = codec, N, K, T_max
+        dev = torch.device(device)
+
+        def to_dev(a, dtype):
+            if isinstance(a, np.ndarray):
+                a = torch.from_numpy(np.ascontiguousarray(a).view(dtype))
+            return a.to(dev).contiguous()
+
+        codes = to_dev(codes_canonical, np.uint8)
+        scales = to_dev(scales_fp16, np.int16)
+        nbytes = qgemm_packed_bytes(N, K, codec)
+        if nbytes == 0:
+            raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_packed_bytes")
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        check(qgemm_pack_weights(codec, N, K, codes, scales, self.packed, stream), "qgemm_pack_weights")
+        st, self.plan = qgemm_plan(N, K, codec, T_max)
+        check(st, "qgemm_plan")
+        wsb = qgemm_plan_workspace_bytes(self.plan)
+        self.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+        check(qgemm_plan_bind(self.plan, self.packed, self.workspace, self.workspace.numel()), "qgemm_plan_bind")
+
+    def route(self, T: int) -> str:
+        return qgemm_route_name(qgemm_plan_route(self.plan, T))
+
+    def run(self, X, Y=None, stream=None):
+        """Y[T, N] fp32 = X[T, K] (bf16) . deq(W)^T."""
+        import torch
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.N), dtype=torch.float32, device=X.device)
+        check(qgemm_run(self.plan, X, T, Y, stream), "qgemm_run")
+        return Y
+
+    def close(self):
+        if getattr(self, "plan", None):
+            qgemm_plan_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def run_multi(weights, X, Ys=None, stream=None):
+    """Several GroupwiseWeights (same K) over one shared X in one launch."""
+    import torch
+    T = X.shape[0]
+    if Ys is None:
+        Ys = [torch.empty((T, w.N), dtype=torch.float32, device=X.device) for w in weights]
+    check(qgemm_run_multi([w.plan for w in weights], X, T, Ys, stream), "qgemm_run_multi")
+    return Ys

@@ -1,0 +1,291 @@
+// C-ABI of the qgemm library: argument validation, plans, route choice and
+// launches.  Declarations and the contract of every entry point are in
+// include/qgemm.h.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/qgemm.h"
+#include "qgemm_internal.cuh"
+
+namespace qg {
+cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16_t *scales, void *out,
+                        cudaStream_t stream);
+cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int grid, cudaStream_t stream);
+}  // namespace qg
+
+using namespace qg;
+
+// ---------------------------------------------------------------- routes
+
+enum Route : int {
+    ROUTE_SKINNY8 = 0,     // weight-streaming split-K, 8-token MMA tile
+    ROUTE_SKINNY16 = 1,    // 16-token tile
+    ROUTE_SKINNY32 = 2,    // 32-token tile
+    ROUTE_SLABS32 = 3,     // wide T as successive 32-token skinny launches
+    ROUTE_COUNT
+};
+
+static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "slabs32"};
+
+static int route_tokens(int route) {
+    switch (route) {
+        case ROUTE_SKINNY8: return 8;
+        case ROUTE_SKINNY16: return 16;
+        default: return 32;
+    }
+}
+
+// Narrowest tile that covers T (the padded width sets the cost, not the live
+// column count).
+static int choose_route(int T) {
+    if (T <= 8) return ROUTE_SKINNY8;
+    if (T <= 16) return ROUTE_SKINNY16;
+    if (T <= 32) return ROUTE_SKINNY32;
+    return ROUTE_SLABS32;
+}
+
+struct qgemm_plan_s {
+    int N, K, codec, T_max;
+    int G, NB, UB;
+    int sms;
+    int S;                 // K splits of the skinny routes
+    int tpad_max;          // widest skinny tile any T <= T_max uses
+    size_t counters_bytes;
+    size_t ws_bytes;
+    const uint8_t *packed;
+    uint8_t *ws;
+    bool bound;
+};
+
+static std::atomic<uint64_t> g_launches{0};
+
+// Device status word (QGEMM_OK or QGEMM_ERR_TIMEOUT); kernels get its address.
+__device__ unsigned int g_device_status = 0;
+
+// Address of the status word on the current device, looked up once per device
+// (the lookup is not a stream operation, so later calls may be captured).
+static unsigned int *status_ptr() {
+    constexpr int MAX_DEVICES = 64;
+    static std::atomic<unsigned int *> cache[MAX_DEVICES];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    unsigned int *p = cache[dev].load();
+    if (p) return p;
+    void *raw = nullptr;
+    if (cudaGetSymbolAddress(&raw, g_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    cache[dev].store(static_cast<unsigned int *>(raw));
+    return static_cast<unsigned int *>(raw);
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5; }
+
+extern "C" {
+
+const char *qgemm_status_string(qgemm_status st) {
+    switch (st) {
+        case QGEMM_OK: return "ok";
+        case QGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case QGEMM_ERR_SHAPE: return "invalid shape";
+        case QGEMM_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
+        case QGEMM_ERR_T_OUT_OF_DOMAIN: return "T outside the plan's domain";
+        case QGEMM_ERR_WORKSPACE: return "workspace missing or too small";
+        case QGEMM_ERR_CUDA: return "CUDA error";
+        case QGEMM_ERR_TIMEOUT: return "device-side wait timed out";
+        case QGEMM_ERR_UNSUPPORTED: return "no supported GPU";
+    }
+    return "unknown status";
+}
+
+size_t qgemm_packed_bytes(int N, int K, qgemm_codec codec) {
+    if (!valid_codec(codec) || N < 1 || K < GROUP || K % GROUP) return 0;
+    const size_t NB = (size_t)(N + BLOCK_ROWS - 1) / BLOCK_ROWS;
+    return NB * (size_t)(K / GROUP) * (size_t)unit_bytes(codec);
+}
+
+qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K, const void *codes_canonical_dev,
+                                const uint16_t *scales_fp16_dev, void *packed_dev, qgemm_stream_t stream) {
+    if (!valid_codec(codec)) return QGEMM_ERR_INVALID_ARG;
+    if (N < 1 || K < GROUP || K % GROUP) return QGEMM_ERR_SHAPE;
+    if (!codes_canonical_dev || !scales_fp16_dev || !packed_dev) return QGEMM_ERR_INVALID_ARG;
+    if (!aligned16(packed_dev)) return QGEMM_ERR_ALIGNMENT;
+    if (launch_pack(codec, N, K, codes_canonical_dev, scales_fp16_dev, packed_dev, (cudaStream_t)stream) !=
+        cudaSuccess)
+        return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out) {
+    if (!out) return QGEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!valid_codec(codec) || T_max < 1) return QGEMM_ERR_INVALID_ARG;
+    if (N < 1 || K < GROUP || K % GROUP) return QGEMM_ERR_SHAPE;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+        cudaGetLastError();
+        return QGEMM_ERR_UNSUPPORTED;
+    }
+    qgemm_plan_s *p = new (std::nothrow) qgemm_plan_s();
+    if (!p) return QGEMM_ERR_INVALID_ARG;
+    p->N = N;
+    p->K = K;
+    p->codec = codec;
+    p->T_max = T_max;
+    p->G = K / GROUP;
+    p->NB = (N + BLOCK_ROWS - 1) / BLOCK_ROWS;
+    p->UB = unit_bytes(codec);
+    p->sms = sms;
+    // Split K so that about four CTAs per SM stream at once, each CTA keeping
+    // at least two groups.
+    const int target = 4 * sms;
+    int S = (target + p->NB - 1) / p->NB;
+    if (S > p->G / 2) S = p->G / 2;
+    if (S < 1) S = 1;
+    p->S = S;
+    const int widest = choose_route(T_max);
+    p->tpad_max = route_tokens(widest);
+    p->counters_bytes = ((size_t)p->NB * sizeof(unsigned int) + 255) / 256 * 256;
+    p->ws_bytes = S > 1 ? p->counters_bytes + (size_t)p->NB * S * p->tpad_max * BLOCK_ROWS * sizeof(float) : 0;
+    *out = p;
+    return QGEMM_OK;
+}
+
+size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan) { return plan ? plan->ws_bytes : 0; }
+
+qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev, void *workspace_dev, size_t ws_bytes) {
+    if (!plan || !packed_dev) return QGEMM_ERR_INVALID_ARG;
+    if (!aligned16(packed_dev)) return QGEMM_ERR_ALIGNMENT;
+    if (plan->ws_bytes) {
+        if (!workspace_dev || ws_bytes < plan->ws_bytes) return QGEMM_ERR_WORKSPACE;
+        if (!aligned16(workspace_dev)) return QGEMM_ERR_ALIGNMENT;
+    }
+    plan->packed = static_cast<const uint8_t *>(packed_dev);
+    plan->ws = static_cast<uint8_t *>(workspace_dev);
+    plan->bound = true;
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_plan_destroy(qgemm_plan_t plan) {
+    delete plan;
+    return QGEMM_OK;
+}
+
+int qgemm_plan_route(qgemm_plan_t plan, int T) {
+    if (!plan || T < 1 || T > plan->T_max) return -1;
+    return choose_route(T);
+}
+
+const char *qgemm_route_name(int route) {
+    return (route >= 0 && route < ROUTE_COUNT) ? kRouteNames[route] : "none";
+}
+
+uint64_t qgemm_launch_count(void) { return g_launches.load(); }
+
+qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof v, 0, cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+        return QGEMM_ERR_CUDA;
+    if (clear && v) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                    (cudaStream_t)stream) != cudaSuccess ||
+            cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+            return QGEMM_ERR_CUDA;
+    }
+    return v ? (qgemm_status)v : QGEMM_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- runs
+
+static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, float *Y, int cta_begin) {
+    sp.packed = p->packed;
+    sp.Y = Y;
+    sp.counters = reinterpret_cast<unsigned int *>(p->ws);
+    sp.partials = p->ws ? reinterpret_cast<float *>(p->ws + p->counters_bytes) : nullptr;
+    sp.N = p->N;
+    sp.NB = p->NB;
+    sp.S = p->S;
+    sp.codec = p->codec;
+    sp.cta_begin = cta_begin;
+}
+
+// One or more parents over the same X; T columns starting at column t0.
+static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
+                                float *const *Ys, cudaStream_t stream) {
+    const int route = choose_route(T);
+    const int K = plans[0]->K;
+    const int slab = route == ROUTE_SLABS32 ? 32 : T;
+    const int nt = route_tokens(route) / 8;
+    for (int t0 = 0; t0 < T; t0 += slab) {
+        const int Ts = (T - t0) < slab ? (T - t0) : slab;
+        SkinnyArgs a;
+        memset(&a, 0, sizeof a);
+        int grid = 0;
+        for (int i = 0; i < np; ++i) {
+            fill_parent(a.p[i], plans[i], Ys[i] + (size_t)t0 * plans[i]->N, grid);
+            grid += plans[i]->NB * plans[i]->S;
+        }
+        a.nparents = np;
+        a.status = status_ptr();
+        if (!a.status) return QGEMM_ERR_CUDA;
+        a.X = reinterpret_cast<const __nv_bfloat16 *>(X) + (size_t)t0 * K;
+        a.T = Ts;
+        a.K = K;
+        a.G = K / GROUP;
+        if (launch_skinny(a, nt, grid, stream) != cudaSuccess)
+            return QGEMM_ERR_CUDA;
+        g_launches.fetch_add(1);
+    }
+    return QGEMM_OK;
+}
+
+static qgemm_status check_run(const qgemm_plan_s *p, const void *X, int T, const float *Y) {
+    if (!p || !p->bound) return QGEMM_ERR_INVALID_ARG;
+    if (T < 0) return QGEMM_ERR_INVALID_ARG;
+    if (T > p->T_max) return QGEMM_ERR_T_OUT_OF_DOMAIN;
+    if (T == 0) return QGEMM_OK;
+    if (!X || !Y) return QGEMM_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y)) return QGEMM_ERR_ALIGNMENT;
+    if (p->ws_bytes && !p->ws) return QGEMM_ERR_WORKSPACE;
+    return QGEMM_OK;
+}
+
+extern "C" qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_stream_t stream) {
+    const qgemm_status st = check_run(plan, X, T, Y);
+    if (st != QGEMM_OK || T == 0) return st;
+    const qgemm_plan_s *plans[1] = {plan};
+    float *Ys[1] = {Y};
+    return run_parents(plans, 1, X, T, Ys, (cudaStream_t)stream);
+}
+
+extern "C" qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
+                                        float *const *Ys, qgemm_stream_t stream) {
+    if (!plans || !Ys || n_parents < 1 || n_parents > MAX_PARENTS) return QGEMM_ERR_INVALID_ARG;
+    for (int i = 0; i < n_parents; ++i) {
+        if (!plans[i]) return QGEMM_ERR_INVALID_ARG;
+        if (plans[i]->K != plans[0]->K) return QGEMM_ERR_SHAPE;
+        for (int j = 0; j < i; ++j)
+            if (plans[j] == plans[i]) return QGEMM_ERR_INVALID_ARG;   // one workspace per parent
+        const qgemm_status st = check_run(plans[i], X, T, Ys[i]);
+        if (st != QGEMM_OK) return st;
+    }
+    if (T == 0) return QGEMM_OK;
+    const qgemm_plan_s *ps[MAX_PARENTS];
+    for (int i = 0; i < n_parents; ++i) ps[i] = plans[i];
+    return run_parents(ps, n_parents, X, T, Ys, (cudaStream_t)stream);
+}

@@ -1,0 +1,166 @@
+// Internal definitions shared by the qgemm CUDA translation units: the packed
+// device layout, kernel parameter blocks and small PTX wrappers (mbarrier,
+// bulk async copies, bf16 tensor-core MMA).
+//
+// Packed device layout ("units").  Rows are grouped in blocks of 128 (eight
+// 16-row tiles); K in groups of 64.  Unit (b, g) holds block b's 128 x 64 codes
+// and their 128 scales, and units are stored block-major:
+//     offset(b, g) = (b * G + g) * UNIT_BYTES(codec)
+// so the units of one block and a run of groups are one contiguous span, which
+// a kernel streams with a few bulk copies.  Inside a unit:
+//   [nibble plane: 8 tiles x 32 lanes x 16 B][int5 only: high-bit plane:
+//    8 tiles x 32 lanes x 4 B][scales: 8 tiles x 8 pairs x 2 x fp16]
+// Lane l = 4*g + c of tile w owns rows r0 = 16w + g and r1 = r0 + 8 and the 16
+// consecutive k = 16c .. 16c+15 of the group:
+//   word 0: r0, k 16c+0..7    word 1: r0, k 16c+8..15
+//   word 2: r1, k 16c+0..7    word 3: r1, k 16c+8..15
+// Inside a word, k offset j sits in nibble position (j >> 1) + 4 * (j & 1), so
+// nibble positions (i, i+4) hold the k pair (2i, 2i+1): masking the word
+// shifted right by 4i with 0x000F000F yields that pair in the two 16-bit
+// halves.  Nibbles hold the biased code u = q + 8 (int4) or the low 4 bits of
+// u = q + 16 (int5).  The int5 high bit of word m, nibble position p sits in
+// bit 4m + p (p < 4) or 16 + 4m + (p - 4) (p >= 4) of the lane's high word.
+// Scale pair i of tile w is (s[16w + i], s[16w + i + 8]).
+// Rows n >= N (padding of the last block) hold u = bias (q = 0) and s = 0.
+//
+// Decode: OR a biased code into the mantissa of bf16 128.0 (0x4300; the
+// mantissa of [128, 256) counts in steps of 1) and subtract 128 + bias: the
+// result is the exact integer q as bf16, with no integer-to-float conversion.
+// This is the magic-number conversion the Q4 small-T MMA of "ninfer-3080
+// docs/performance.md" (small-T kernels section) describes.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace qg {
+
+constexpr int GROUP = 64;
+constexpr int BLOCK_ROWS = 128;
+constexpr int TILES = 8;                   // 16-row tiles per block
+constexpr int NIB_BYTES = 4096;            // nibble plane of a unit
+constexpr int HI_BYTES = 1024;             // int5 high-bit plane of a unit
+constexpr int SCALE_BYTES = 256;           // 128 fp16 scales
+constexpr int UNIT4 = NIB_BYTES + SCALE_BYTES;
+constexpr int UNIT5 = NIB_BYTES + HI_BYTES + SCALE_BYTES;
+
+__host__ __device__ constexpr int unit_bytes(int codec) { return codec == 5 ? UNIT5 : UNIT4; }
+__host__ __device__ constexpr int scale_off(int codec) { return codec == 5 ? NIB_BYTES + HI_BYTES : NIB_BYTES; }
+
+// nibble position of k offset j (0..7) inside a code word
+__host__ __device__ constexpr int nib_pos(int j) { return (j >> 1) + 4 * (j & 1); }
+// bit of the lane's high word holding the int5 high bit of word m, nibble position p
+__host__ __device__ constexpr int hi_bit(int m, int p) { return p < 4 ? 4 * m + p : 16 + 4 * m + (p - 4); }
+
+// ---------------------------------------------------------------- device status
+
+// Kernels receive the address of the library's device status word and set it
+// to QGEMM_ERR_TIMEOUT when a bounded wait gives up.
+
+constexpr long long SPIN_LIMIT = 1ll << 22;   // polls of one mbarrier wait (well under seconds)
+
+// ---------------------------------------------------------------- kernel parameters
+
+constexpr int MAX_PARENTS = 4;
+
+struct SkinnyParent {
+    const uint8_t *packed;   // units of this parent
+    float *Y;                // [T][N]
+    float *partials;         // [NB][S][tpad][128] (S > 1)
+    unsigned int *counters;  // [NB] (S > 1)
+    int N, NB, S, codec;
+    int cta_begin;           // first CTA of this parent in the grid
+};
+
+struct SkinnyArgs {
+    SkinnyParent p[MAX_PARENTS];
+    int nparents;
+    const __nv_bfloat16 *X;  // [T][K]
+    int T, K, G;
+    unsigned int *status;    // device status word
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false (and the device
+// status set to timeout) if it did not complete within SPIN_LIMIT polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    for (long long i = 0; i < SPIN_LIMIT; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicExch(status, 7u /* QGEMM_ERR_TIMEOUT */);
+    return false;
+}
+
+// 1-D bulk async copy global -> shared, completion counted on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// D = A * B + C, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], const uint32_t b[2],
+                                               const float c[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]),
+          "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// bf16x2 subtract (exact here: both halves are small integers)
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Codes (i, i+4) of a nibble word as an exact bf16x2 pair of integers.
+template <int SHIFT>
+__device__ __forceinline__ uint32_t dec4_pair(uint32_t w) {
+    return bf16x2_sub(((w >> SHIFT) & 0x000F000Fu) | 0x43004300u, 0x43084308u);   // - (128 + 8)
+}
+
+// int5: nibble pair plus the two high bits taken from the lane's high word.
+template <int SHIFT, int HSH>
+__device__ __forceinline__ uint32_t dec5_pair(uint32_t w, uint32_t h) {
+    uint32_t hb = (HSH >= 0 ? (h >> HSH) : (h << (-HSH))) & 0x00100010u;
+    return bf16x2_sub(((w >> SHIFT) & 0x000F000Fu) | hb | 0x43004300u, 0x43104310u);   // - (128 + 16)
+}
+
+}  // namespace qg

@@ -1,0 +1,168 @@
+/*
+ * qgemm -- groupwise int4/int5 weight-only dequant-GEMM for GB300 (sm_103a).
+ *
+ *     Y[t][n] = sum_k X[t][k] * deq(W)[n][k],   deq(W)[n][k] = s[n][k/64] * q[n][k]
+ *
+ * for t < T token columns, n < N weight rows and k < K input channels.
+ *
+ * The operation is the fused "unpack the weights and multiply them in one pass
+ * shaped for a batch" of "Fused kernels" (ark-labs.cloud research note, section
+ * "Why standard kernels stall"), on the groupwise-int weight format of
+ * "ninfer-3080 docs/performance.md": integer codes with one scale per 64
+ * K-columns per row (cuBLAS prefill route section) in the Q4 and Q5 codecs
+ * (small-T kernels section), evaluated at the decode, speculative-verify,
+ * batched-decode and prefill token widths the same page routes separately
+ * (route boundaries section).
+ *
+ * Number formats
+ *   q  symmetric two's-complement code, no zero point: int4 in [-8, 7],
+ *      int5 in [-16, 15];
+ *   s  IEEE fp16, one per (row, 64-column group); any finite value, negative
+ *      and subnormal included (non-finite scales propagate but the result is
+ *      then unspecified beyond being non-finite);
+ *   X  bf16, row-major [T][K] (K contiguous);
+ *   Y  fp32, row-major [T][N] (N contiguous), overwritten (no accumulate).
+ *   s * q is never rounded: products run on the exact integer codes and each
+ *   group's fp32 partial sum is multiplied by its scale.  Accumulation is fp32.
+ *
+ * Canonical packed codes (the input of qgemm_pack_weights)
+ *   int4: K/2 bytes per row, row-major; byte j holds code 2j in bits 0-3 and
+ *         code 2j+1 in bits 4-7.
+ *   int5: 5K/8 bytes per row, row-major; LSB-first bitstream, code k in bits
+ *         5k .. 5k+4.
+ *   scales: fp16 bit patterns, row-major [N][K/64].
+ *
+ * Conventions for every call
+ *   - All pointers named *_dev and X, Y are device pointers (or managed /
+ *     mapped memory the GPU can reach).  The caller allocates and owns every
+ *     buffer; the library owns only the host-side plan object.
+ *   - Everything is asynchronous on the given stream (0 = legacy default
+ *     stream); no call synchronises the device.
+ *   - Argument errors return a status before anything is launched; a launch
+ *     failure returns QGEMM_ERR_CUDA.  Nothing aborts, no C++ exception crosses
+ *     this interface.
+ *   - Results are bitwise repeatable for a given (plan, T); different T may
+ *     take different routes and summation orders and then agree only within
+ *     the fp32 rounding tolerance.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qgemm_stream_t;   /* a cudaStream_t */
+
+typedef enum {
+    QGEMM_OK = 0,
+    QGEMM_ERR_INVALID_ARG = 1,     /* null pointer, unknown codec, negative size, plan not bound */
+    QGEMM_ERR_SHAPE = 2,           /* K not a positive multiple of 64, N < 1, shapes of parents differ */
+    QGEMM_ERR_ALIGNMENT = 3,       /* a buffer is not 16-byte aligned */
+    QGEMM_ERR_T_OUT_OF_DOMAIN = 4, /* T larger than the plan's T_max */
+    QGEMM_ERR_WORKSPACE = 5,       /* workspace missing or smaller than qgemm_plan_workspace_bytes */
+    QGEMM_ERR_CUDA = 6,            /* a CUDA call or launch failed */
+    QGEMM_ERR_TIMEOUT = 7,         /* a bounded device-side wait ran out (see qgemm_device_status) */
+    QGEMM_ERR_UNSUPPORTED = 8      /* no usable GPU of the architecture this library was built for */
+} qgemm_status;
+
+typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5 } qgemm_codec;
+
+typedef struct qgemm_plan_s *qgemm_plan_t;
+
+/* Human-readable name of a status (static string, never NULL). */
+const char *qgemm_status_string(qgemm_status st);
+
+/*
+ * Bytes of the device-side packed weight buffer for an N x K matrix of the
+ * given codec, or 0 for an invalid shape (K not a positive multiple of 64,
+ * N < 1, unknown codec).  Rows are padded to a multiple of 128.
+ */
+size_t qgemm_packed_bytes(int N, int K, qgemm_codec codec);
+
+/*
+ * Repack canonical codes and fp16 scales into the library's device layout
+ * (one launch on `stream`).  Weight-only quantised serving packs each matrix
+ * once at load time; the layout is private to the library and shared by all
+ * of its routes.
+ *   codes_canonical_dev  canonical packed codes, N rows (see above)
+ *   scales_fp16_dev      fp16 patterns [N][K/64]
+ *   packed_dev           qgemm_packed_bytes(N, K, codec) bytes, 16-byte aligned
+ * The inputs may be freed once the stream has passed the launch.
+ */
+qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
+                                const void *codes_canonical_dev,
+                                const uint16_t *scales_fp16_dev,
+                                void *packed_dev, qgemm_stream_t stream);
+
+/*
+ * Host-only: choose the routes for an N x K matrix and token widths
+ * 1 .. T_max from the built-in route table (measured per token width; the
+ * "ninfer-3080 docs/performance.md" route boundaries section explains why
+ * boundaries must come from measurement).  Queries the current device's SM
+ * count; launches nothing.  *out must be released with qgemm_plan_destroy.
+ */
+qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out);
+
+/* Workspace bytes the plan needs at its T_max (0 if none). */
+size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan);
+
+/*
+ * Attach the packed weights and the workspace to a plan.  The workspace must
+ * be zero-filled before its first use (the library leaves it zeroed after
+ * every completed run).  Runs that share one plan, and hence one workspace,
+ * must not overlap on the GPU.  ws_bytes may exceed the requirement.
+ */
+qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev,
+                             void *workspace_dev, size_t ws_bytes);
+
+/*
+ * Y[T][N] = X[T][K] . deq(W)^T on `stream`.  X (bf16 bit patterns) and Y
+ * must be 16-byte aligned.  T == 0 is a no-op; T > T_max returns
+ * QGEMM_ERR_T_OUT_OF_DOMAIN.
+ */
+qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_stream_t stream);
+
+/*
+ * Several weight matrices ("parents") over one shared activation X in a
+ * single launch, as the two-parent projections of "ninfer-3080
+ * docs/performance.md" (A8 prefill routes section: two parents over one
+ * activation share its preparation).  All plans must have the same K and
+ * T <= each plan's T_max; codecs may differ.  Ys[i] receives parent i's
+ * [T][N_i] result.  1 <= n_parents <= 4.
+ */
+qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
+                             float *const *Ys, qgemm_stream_t stream);
+
+/* Release a plan (NULL is accepted). */
+qgemm_status qgemm_plan_destroy(qgemm_plan_t plan);
+
+/*
+ * Route the plan takes at width T (a small integer naming the kernel family
+ * and its tile width, see qgemm_route_name), or -1 if T is outside 1..T_max.
+ */
+int qgemm_plan_route(qgemm_plan_t plan, int T);
+const char *qgemm_route_name(int route);
+
+/*
+ * Number of kernels this library has launched since it was loaded (host
+ * counter), so that callers and tests can check that one call runs exactly
+ * the kernels its route names.
+ */
+uint64_t qgemm_launch_count(void);
+
+/*
+ * Device-side status word: QGEMM_OK, or QGEMM_ERR_TIMEOUT after a bounded
+ * wait inside a kernel ran out (the kernel then skipped its remaining work
+ * and returned).  Synchronises `stream` to read it; `clear` resets it.
+ */
+qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

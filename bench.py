@@ -269,6 +269,7 @@ def run_ours(args, desc):
             wsb = qg.qgemm_plan_workspace_bytes(w.plan)
             w.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
             qg.check(qg.qgemm_plan_bind(w.plan, w.packed, w.workspace, w.workspace.numel()), "bind")
+            qg.check(qg.qgemm_plan_set_pdl(w.plan, not args.no_pdl), "set_pdl")
             ws.append(w)
         weight_sets.append(ws)
     xs = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).to(dev) for T in Ts}
@@ -405,7 +406,8 @@ def run_ours(args, desc):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc["name"], "parents": desc["parents"], "K": desc["K"], "T": Ts,
                        "l2": f"rotating {copies} packed-weight copies ({copies * set_bytes / 1e6:.0f} MB > 3x L2)",
-                       "parallelism": "replicas" if world > 1 else "single"},
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "pdl": not args.no_pdl},
             "per_T": per_T,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
@@ -430,6 +432,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=6.0)

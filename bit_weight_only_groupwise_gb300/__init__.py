@@ -38,7 +38,7 @@ EXPORTS = [
     "qgemm_status_string", "qgemm_packed_bytes", "qgemm_pack_weights", "qgemm_plan",
     "qgemm_plan_workspace_bytes", "qgemm_plan_bind", "qgemm_run", "qgemm_run_multi",
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
-    "qgemm_device_status",
+    "qgemm_device_status", "qgemm_plan_set_pdl",
 ]
 
 _lock = threading.Lock()
@@ -68,6 +68,7 @@ def _declare(lib):
         "qgemm_route_name": ([i32], c.c_char_p),
         "qgemm_launch_count": ([], u64),
         "qgemm_device_status": ([vp, i32], i32),
+        "qgemm_plan_set_pdl": ([vp, i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -153,6 +154,10 @@ def qgemm_run_multi(plans, X, T: int, Ys, stream=None) -> int:
 
 def qgemm_plan_destroy(plan) -> int:
     return load().qgemm_plan_destroy(plan)
+
+
+def qgemm_plan_set_pdl(plan, enable: bool) -> int:
+    return load().qgemm_plan_set_pdl(plan, 1 if enable else 0)
 
 
 def qgemm_plan_route(plan, T: int) -> int:

@@ -6,13 +6,14 @@
 #include <cstring>
 #include <new>
 
-#include "../../include/qgemm.h"
+#include "qgemm.h"
 #include "qgemm_internal.cuh"
 
 namespace qg {
 cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16_t *scales, void *out,
                         cudaStream_t stream);
-cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int grid, cudaStream_t stream);
+cudaError_t launch_fence(cudaStream_t stream);
+cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
 }  // namespace qg
 
 using namespace qg;
@@ -50,10 +51,8 @@ struct qgemm_plan_s {
     int N, K, codec, T_max;
     int G, NB, UB;
     int sms;
-    int S;                 // K splits of the skinny routes
-    int tpad_max;          // widest skinny tile any T <= T_max uses
-    size_t counters_bytes;
-    size_t ws_bytes;
+    bool pdl;              // launch with programmatic dependent launch
+    size_t ws_bytes;       // workspace the plan's routes need (none so far)
     const uint8_t *packed;
     uint8_t *ws;
     bool bound;
@@ -121,7 +120,11 @@ qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K, const void *cod
     if (launch_pack(codec, N, K, codes_canonical_dev, scales_fp16_dev, packed_dev, (cudaStream_t)stream) !=
         cudaSuccess)
         return QGEMM_ERR_CUDA;
-    g_launches.fetch_add(1);
+    // Runs prefetch weights before their programmatic wait on the preceding
+    // kernel; an empty kernel after the pack keeps the pack's writes complete
+    // before any run on this stream can start.
+    if (launch_fence((cudaStream_t)stream) != cudaSuccess) return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(2);
     return QGEMM_OK;
 }
 
@@ -146,17 +149,8 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     p->NB = (N + BLOCK_ROWS - 1) / BLOCK_ROWS;
     p->UB = unit_bytes(codec);
     p->sms = sms;
-    // Split K so that about four CTAs per SM stream at once, each CTA keeping
-    // at least two groups.
-    const int target = 4 * sms;
-    int S = (target + p->NB - 1) / p->NB;
-    if (S > p->G / 2) S = p->G / 2;
-    if (S < 1) S = 1;
-    p->S = S;
-    const int widest = choose_route(T_max);
-    p->tpad_max = route_tokens(widest);
-    p->counters_bytes = ((size_t)p->NB * sizeof(unsigned int) + 255) / 256 * 256;
-    p->ws_bytes = S > 1 ? p->counters_bytes + (size_t)p->NB * S * p->tpad_max * BLOCK_ROWS * sizeof(float) : 0;
+    p->pdl = true;
+    p->ws_bytes = 0;
     *out = p;
     return QGEMM_OK;
 }
@@ -178,6 +172,12 @@ qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev, void *wo
 
 qgemm_status qgemm_plan_destroy(qgemm_plan_t plan) {
     delete plan;
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable) {
+    if (!plan) return QGEMM_ERR_INVALID_ARG;
+    plan->pdl = enable != 0;
     return QGEMM_OK;
 }
 
@@ -215,22 +215,31 @@ qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear) {
 static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, float *Y, int cta_begin) {
     sp.packed = p->packed;
     sp.Y = Y;
-    sp.counters = reinterpret_cast<unsigned int *>(p->ws);
-    sp.partials = p->ws ? reinterpret_cast<float *>(p->ws + p->counters_bytes) : nullptr;
     sp.N = p->N;
-    sp.NB = p->NB;
-    sp.S = p->S;
     sp.codec = p->codec;
     sp.cta_begin = cta_begin;
 }
 
-// One or more parents over the same X; T columns starting at column t0.
+// Tuning knob read once from the environment, for sweeps only:
+// QGEMM_SKINNY_WARPS sets the warps (K slices) per CTA of the small-T route.
+static int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+
+// One or more parents over the same X (all T columns; wide T in 32-column slabs).
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
                                 float *const *Ys, cudaStream_t stream) {
+    static const int kw = env_int("QGEMM_SKINNY_WARPS", 8);
     const int route = choose_route(T);
     const int K = plans[0]->K;
+    const int G = K / GROUP;
     const int slab = route == ROUTE_SLABS32 ? 32 : T;
     const int nt = route_tokens(route) / 8;
+    bool pdl = true;
+    for (int i = 0; i < np; ++i) pdl = pdl && plans[i]->pdl;
+    unsigned int *status = status_ptr();
+    if (!status) return QGEMM_ERR_CUDA;
     for (int t0 = 0; t0 < T; t0 += slab) {
         const int Ts = (T - t0) < slab ? (T - t0) : slab;
         SkinnyArgs a;
@@ -238,17 +247,15 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
         int grid = 0;
         for (int i = 0; i < np; ++i) {
             fill_parent(a.p[i], plans[i], Ys[i] + (size_t)t0 * plans[i]->N, grid);
-            grid += plans[i]->NB * plans[i]->S;
+            grid += (plans[i]->N + 15) / 16;
         }
         a.nparents = np;
-        a.status = status_ptr();
-        if (!a.status) return QGEMM_ERR_CUDA;
+        a.status = status;
         a.X = reinterpret_cast<const __nv_bfloat16 *>(X) + (size_t)t0 * K;
         a.T = Ts;
         a.K = K;
-        a.G = K / GROUP;
-        if (launch_skinny(a, nt, grid, stream) != cudaSuccess)
-            return QGEMM_ERR_CUDA;
+        a.G = G;
+        if (launch_skinny(a, nt, kw, grid, pdl, stream) != cudaSuccess) return QGEMM_ERR_CUDA;
         g_launches.fetch_add(1);
     }
     return QGEMM_OK;

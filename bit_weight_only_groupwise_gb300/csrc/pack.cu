@@ -63,4 +63,11 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
     return cudaGetLastError();
 }
 
+__global__ void fence_kernel() {}
+
+cudaError_t launch_fence(cudaStream_t stream) {
+    fence_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 }  // namespace qg

@@ -68,12 +68,11 @@ constexpr int MAX_PARENTS = 4;
 struct SkinnyParent {
     const uint8_t *packed;   // units of this parent
     float *Y;                // [T][N]
-    float *partials;         // [NB][S][tpad][128] (S > 1)
-    unsigned int *counters;  // [NB] (S > 1)
-    int N, NB, S, codec;
+    int N, codec;
     int cta_begin;           // first CTA of this parent in the grid
 };
 
+// The grid has one CTA per 16-row tile of every parent (ceil(N/16) each).
 struct SkinnyArgs {
     SkinnyParent p[MAX_PARENTS];
     int nparents;
@@ -124,6 +123,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     return false;
 }
 
+// Streaming global loads of read-once data: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// 16-byte asynchronous global -> shared copy (L2 only), committed in groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // 1-D bulk async copy global -> shared, completion counted on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -141,6 +171,19 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], 
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]),
           "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// ---- programmatic dependent launch
+
+// Let the next kernel in the stream start launching its CTAs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel in the stream has completed and its memory
+// is visible (a no-op when launched without a programmatic dependency).
+__device__ __forceinline__ void pdl_wait_prior() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // bf16x2 subtract (exact here: both halves are small integers)

@@ -107,7 +107,8 @@ qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
  */
 qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out);
 
-/* Workspace bytes the plan needs at its T_max (0 if none). */
+/* Workspace bytes the plan needs at its T_max (0 if none; the current
+ * routes combine their K splits on chip and need none). */
 size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan);
 
 /*
@@ -139,6 +140,17 @@ qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const voi
 
 /* Release a plan (NULL is accepted). */
 qgemm_status qgemm_plan_destroy(qgemm_plan_t plan);
+
+/*
+ * Programmatic dependent launch (enabled by default): a run's kernel may be
+ * scheduled while the preceding kernel on the stream is still draining and
+ * prefetches its packed weights before waiting for that kernel to finish; it
+ * reads X and writes Y only after the wait.  So the packed buffer must not
+ * be written by the kernel immediately preceding a run on the same stream
+ * (qgemm_pack_weights itself ends with an empty kernel for this reason).
+ * enable = 0 turns it off for runs of this plan.
+ */
+qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable);
 
 /*
  * Route the plan takes at width T (a small integer naming the kernel family

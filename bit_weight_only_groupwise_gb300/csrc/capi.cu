@@ -14,6 +14,15 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
                         cudaStream_t stream);
 cudaError_t launch_fence(cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
+struct WideParent {
+    const uint8_t *packed;
+    float *Y;
+    int N, codec;
+    int cta_begin;
+    int nblocks;
+};
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
+                        cudaStream_t stream);
 }  // namespace qg
 
 using namespace qg;
@@ -21,20 +30,21 @@ using namespace qg;
 // ---------------------------------------------------------------- routes
 
 enum Route : int {
-    ROUTE_SKINNY8 = 0,     // weight-streaming split-K, 8-token MMA tile
+    ROUTE_SKINNY8 = 0,     // weight-streaming skinny GEMM, 8-token MMA tile
     ROUTE_SKINNY16 = 1,    // 16-token tile
     ROUTE_SKINNY32 = 2,    // 32-token tile
-    ROUTE_SLABS32 = 3,     // wide T as successive 32-token skinny launches
+    ROUTE_WIDE128 = 3,     // tcgen05 tiles of 128 rows x 128 tokens
     ROUTE_COUNT
 };
 
-static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "slabs32"};
+static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "tcgen05_128x128"};
 
 static int route_tokens(int route) {
     switch (route) {
         case ROUTE_SKINNY8: return 8;
         case ROUTE_SKINNY16: return 16;
-        default: return 32;
+        case ROUTE_SKINNY32: return 32;
+        default: return 128;
     }
 }
 
@@ -44,7 +54,7 @@ static int choose_route(int T) {
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
     if (T <= 32) return ROUTE_SKINNY32;
-    return ROUTE_SLABS32;
+    return ROUTE_WIDE128;
 }
 
 struct qgemm_plan_s {
@@ -227,37 +237,45 @@ static int env_int(const char *name, int dflt) {
     return (v && *v) ? atoi(v) : dflt;
 }
 
-// One or more parents over the same X (all T columns; wide T in 32-column slabs).
+// One or more parents over the same X in one launch of the route T selects.
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
                                 float *const *Ys, cudaStream_t stream) {
     static const int kw = env_int("QGEMM_SKINNY_WARPS", 8);
     const int route = choose_route(T);
     const int K = plans[0]->K;
     const int G = K / GROUP;
-    const int slab = route == ROUTE_SLABS32 ? 32 : T;
-    const int nt = route_tokens(route) / 8;
-    bool pdl = true;
-    for (int i = 0; i < np; ++i) pdl = pdl && plans[i]->pdl;
     unsigned int *status = status_ptr();
     if (!status) return QGEMM_ERR_CUDA;
-    for (int t0 = 0; t0 < T; t0 += slab) {
-        const int Ts = (T - t0) < slab ? (T - t0) : slab;
-        SkinnyArgs a;
-        memset(&a, 0, sizeof a);
-        int grid = 0;
+    if (route == ROUTE_WIDE128) {
+        WideParent wp[MAX_PARENTS];
+        memset(wp, 0, sizeof wp);
         for (int i = 0; i < np; ++i) {
-            fill_parent(a.p[i], plans[i], Ys[i] + (size_t)t0 * plans[i]->N, grid);
-            grid += (plans[i]->N + 15) / 16;
+            wp[i].packed = plans[i]->packed;
+            wp[i].Y = Ys[i];
+            wp[i].N = plans[i]->N;
+            wp[i].codec = plans[i]->codec;
         }
-        a.nparents = np;
-        a.status = status;
-        a.X = reinterpret_cast<const __nv_bfloat16 *>(X) + (size_t)t0 * K;
-        a.T = Ts;
-        a.K = K;
-        a.G = G;
-        if (launch_skinny(a, nt, kw, grid, pdl, stream) != cudaSuccess) return QGEMM_ERR_CUDA;
+        if (launch_wide(wp, np, X, T, K, status, stream) != cudaSuccess) return QGEMM_ERR_CUDA;
         g_launches.fetch_add(1);
+        return QGEMM_OK;
     }
+    bool pdl = true;
+    for (int i = 0; i < np; ++i) pdl = pdl && plans[i]->pdl;
+    SkinnyArgs a;
+    memset(&a, 0, sizeof a);
+    int grid = 0;
+    for (int i = 0; i < np; ++i) {
+        fill_parent(a.p[i], plans[i], Ys[i], grid);
+        grid += (plans[i]->N + 15) / 16;
+    }
+    a.nparents = np;
+    a.status = status;
+    a.X = reinterpret_cast<const __nv_bfloat16 *>(X);
+    a.T = T;
+    a.K = K;
+    a.G = G;
+    if (launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, stream) != cudaSuccess) return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(1);
     return QGEMM_OK;
 }
 

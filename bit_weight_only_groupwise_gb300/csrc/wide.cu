@@ -1,0 +1,427 @@
+// Wide-T route: a tcgen05 (5th-generation tensor core) dequant-GEMM.
+//
+// From a few dozen token columns up the operation is a dense contraction and
+// belongs on the tensor cores; prefill widths are compute-bound ("ninfer-3080
+// docs/performance.md", token tile section: the token tile width sets how
+// often the weights are re-streamed, and the per-group rescale and the operand
+// assembly are the costs beside the MMAs).  One CTA computes a 128-row block of
+// Y^T for a 128-token tile:
+//
+//   D[128 rows x 128 tokens] = sum over 64-column groups g of s[:, g] * P_g,
+//   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, 128 x 64)^T
+//
+// Warp roles (16 warps):
+//   warp 0        producer: 1-D bulk copies of the packed weight units and 2-D
+//                 TMA loads of 128B-swizzled activation tiles into smem rings;
+//   warp 1        allocates tensor memory; one lane issues the MMAs;
+//   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
+//                 the group (magic-number bf16 decode, exact) and stores them
+//                 into tensor memory as the A operand (tcgen05.st), so shared
+//                 memory bandwidth is left to the B operand;
+//   warps 8..15   epilogue: read P_g from tensor memory (tcgen05.ld), multiply
+//                 by the row's fp16 scale and accumulate in fp32 registers
+//                 (packed f32x2 FMA), then write Y.
+// Tensor memory: two P buffers of 128 columns (the MMA fills one while the
+// epilogue drains the other) and NA A stages of 32 columns (64 bf16 per row).
+// Every mbarrier wait is bounded; a wait that runs out sets the device status
+// to timeout and the CTA winds down.
+#include <cuda.h>
+
+#include "qgemm_internal.cuh"
+
+namespace qg {
+
+namespace wide {
+
+constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
+constexpr int BN = 128;                   // tokens per CTA (MMA N)
+constexpr int NX = 6;                     // activation tile stages (16 KB each)
+constexpr int NW = 4;                     // weight unit stages
+constexpr int NA = 4;                     // A stages in tensor memory
+constexpr int THREADS = 512;
+constexpr int X_STAGE = BN * GROUP * 2;   // 16 KB
+constexpr int P_COL = 0;                  // P buffers: columns [0, 256)
+constexpr int A_COL = 256;                // A stages: columns [256, 256 + 32*NA)
+constexpr int TMEM_COLS = 512;
+
+struct Smem {
+    static constexpr int X_OFF = 0;                          // 1024-aligned (128B swizzle atoms)
+    static constexpr int W_OFF = X_OFF + NX * X_STAGE;
+    static constexpr int BAR_OFF = W_OFF + NW * UNIT5;
+    static constexpr int NBAR = 2 * NX + 2 * NW + 2 * NA + 2 * 2;
+    static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int BYTES = TADDR_OFF + 16 + 1024;      // + slack to align the base
+};
+
+}  // namespace wide
+
+struct WideParent {
+    const uint8_t *packed;
+    float *Y;
+    int N, codec;
+    int cta_begin;        // first CTA of this parent
+    int nblocks;          // 128-row blocks
+};
+
+struct WideArgs {
+    WideParent p[MAX_PARENTS];
+    int nparents;
+    int T, K, G;
+    int ntt;              // token tiles
+    unsigned int *status;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(tmem) . B(smem desc)^T, bf16 inputs, fp32 accumulate
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool accum) {
+    asm volatile(
+        "{.reg .pred p; setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
+        ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(accum ? 1u : 0u) : "memory");
+}
+
+// arrive on an mbarrier once all previously issued MMAs of this thread complete
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+#define QG_R32(a) a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[8], a[9], a[10], a[11], a[12], a[13], a[14], \
+                  a[15], a[16], a[17], a[18], a[19], a[20], a[21], a[22], a[23], a[24], a[25], a[26], a[27], a[28], \
+                  a[29], a[30], a[31]
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2-D tiled TMA load of box {64 columns, 128 rows} at (x, y) into smem.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as
+// 128-byte rows in 8-row, 1024-byte swizzle atoms (128B swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);          // start address
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                         // descriptor version for this architecture
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+__global__ void __launch_bounds__(wide::THREADS, 1)
+    wide_kernel(const __grid_constant__ WideArgs args, const __grid_constant__ CUtensorMap xmap) {
+    using namespace wide;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *xs = smem + Smem::X_OFF;
+    uint8_t *ws = smem + Smem::W_OFF;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::BAR_OFF);
+    uint64_t *x_full = bars, *x_empty = x_full + NX;
+    uint64_t *w_full = x_empty + NX, *w_empty = w_full + NW;
+    uint64_t *a_full = w_empty + NW, *a_empty = a_full + NA;
+    uint64_t *p_full = a_empty + NA, *p_empty = p_full + 2;
+    volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
+    volatile uint32_t *abort_flag = taddr_slot + 1;
+
+    // ---- which parent, row block and token tile
+    int pi = 0;
+#pragma unroll
+    for (int i = 1; i < MAX_PARENTS; ++i)
+        if (i < args.nparents && (int)blockIdx.x >= args.p[i].cta_begin) pi = i;
+    const WideParent &P = args.p[pi];
+    const int local = blockIdx.x - P.cta_begin;
+    const int blk = local / args.ntt, tt = local % args.ntt;
+    const int G = args.G, T = args.T;
+    const int codec = P.codec;
+    const int UB = unit_bytes(codec);
+    const uint8_t *units = P.packed + (size_t)blk * G * UB;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
+        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
+        for (int i = 0; i < NA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 8); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32((const void *)taddr_slot)), "n"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *taddr_slot;
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            bool ok = true;
+            for (int g = 0; g < G && ok; ++g) {
+                const int wsl = g % NW, xsl = g % NX;
+                if (g >= NW) ok = mbar_wait(&w_empty[wsl], ((g / NW) - 1) & 1, args.status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&w_full[wsl], UB);
+                bulk_g2s(ws + wsl * UNIT5, units + (size_t)g * UB, UB, &w_full[wsl]);
+                if (g >= NX) ok = mbar_wait(&x_empty[xsl], ((g / NX) - 1) & 1, args.status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&x_full[xsl], X_STAGE);
+                tma_load_2d(xs + xsl * X_STAGE, &xmap, g * GROUP, tt * BN, &x_full[xsl]);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16(BM, BN);
+            for (int g = 0; g < G && ok; ++g) {
+                const int asl = g % NA, xsl = g % NX, ps = g & 1;
+                ok = mbar_wait(&a_full[asl], (g / NA) & 1, args.status) &&
+                     mbar_wait(&x_full[xsl], (g / NX) & 1, args.status) &&
+                     (g < 2 || mbar_wait(&p_empty[ps], ((g / 2) - 1) & 1, args.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem + P_COL + ps * BN;
+                const uint32_t a = tmem + A_COL + asl * 32;
+                const uint32_t b0 = smem_u32(xs + xsl * X_STAGE);
+#pragma unroll
+                for (int kk = 0; kk < GROUP / 16; ++kk)
+                    tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
+                tc_commit(&p_full[ps]);
+                tc_commit(&a_empty[asl]);
+                tc_commit(&x_empty[xsl]);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- dequant: thread = weight row r of the block
+        const int q = warp & 3;                   // TMEM lane quarter
+        const int r = q * 32 + lane;
+        const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
+        bool ok = true;
+        for (int g = 0; g < G && ok; ++g) {
+            const int wsl = g % NW, asl = g % NA;
+            ok = mbar_wait(&w_full[wsl], (g / NW) & 1, args.status);
+            if (!ok) break;
+            const uint8_t *u = ws + wsl * UNIT5;
+            uint32_t wd[8];                       // words: (c, 0) k 16c..16c+7, (c, 1) k 16c+8..16c+15
+            uint32_t hw[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
+                wd[2 * c] = v.x;
+                wd[2 * c + 1] = v.y;
+                hw[c] = codec == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
+            // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
+            uint32_t av[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t w = wd[2 * c + h];
+                    uint32_t *o = av + 8 * c + 4 * h;
+                    if (codec == 4) {
+                        o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                    } else {
+                        // this row's words in the lane's high word: m = 2*half + h
+                        const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
+                        o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                        o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                    }
+                }
+            }
+            if (g >= NA) ok = mbar_wait(&a_empty[asl], ((g / NA) - 1) & 1, args.status);
+            if (!ok) break;
+            tc_fence_after();
+            tc_st32(tmem + ((uint32_t)(q * 32) << 16) + A_COL + asl * 32, av);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[asl]);
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 8) {
+        // ---------------- epilogue: thread = row r, columns [64*hc, 64*hc + 64)
+        const int q = warp & 3, hc = (warp - 8) >> 2;
+        const int r = q * 32 + lane;
+        const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
+        const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
+        float2 acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
+        bool ok = true;
+        uint16_t s_next = *reinterpret_cast<const uint16_t *>(units + soff);
+        for (int g = 0; g < G && ok; ++g) {
+            const uint16_t s_bits = s_next;
+            if (g + 1 < G) s_next = *reinterpret_cast<const uint16_t *>(units + (size_t)(g + 1) * UB + soff);
+            const int ps = g & 1;
+            ok = mbar_wait(&p_full[ps], (g / 2) & 1, args.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
+            uint32_t v0[32], v1[32];
+            tc_ld32(base, v0);
+            tc_ld32(base + 32, v1);
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_empty[ps]);
+            const float s = __half2float(__ushort_as_half(s_bits));
+            const float2 s2 = make_float2(s, s);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
+        }
+        if (!ok) *abort_flag = 1;
+        // ---- write Y[t][n] (consecutive lanes = consecutive rows n)
+        const int n = blk * BM + r;
+        if (ok && n < P.N) {
+            const int t0 = tt * BN + hc * 64;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = t0 + 2 * j;
+                if (t < T) P.Y[(size_t)t * P.N + n] = acc[j].x;
+                if (t + 1 < T) P.Y[(size_t)(t + 1) * P.N + n] = acc[j].y;
+            }
+        }
+    }
+
+    // ---- every role is done with tensor memory: release it
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Tensor map of X [T][K] bf16 with {64 columns x 128 rows} boxes, 128B swizzle,
+// zero fill beyond T.
+static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {GROUP, wide::BN};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int wide_tile_tokens() { return wide::BN; }
+
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
+                        cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::Smem::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    CUtensorMap xmap;
+    if ((e = make_xmap(&xmap, X, T, K)) != cudaSuccess) return e;
+    WideArgs a;
+    memset(&a, 0, sizeof a);
+    const int ntt = (T + wide::BN - 1) / wide::BN;
+    int grid = 0;
+    for (int i = 0; i < np; ++i) {
+        a.p[i] = parents[i];
+        a.p[i].cta_begin = grid;
+        a.p[i].nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
+        grid += a.p[i].nblocks * ntt;
+    }
+    a.nparents = np;
+    a.T = T;
+    a.K = K;
+    a.G = K / GROUP;
+    a.ntt = ntt;
+    a.status = status;
+    wide_kernel<<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -185,8 +185,8 @@ def test_one_route_per_call(T):
     n0 = qg.qgemm_launch_count()
     W.run(X)
     launched = qg.qgemm_launch_count() - n0
-    expect = (T + 31) // 32 if route == "slabs32" else 1
-    assert launched == expect, (route, launched)
+    assert launched == 1, (route, launched)
+    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "skinny32" if T <= 32 else "tcgen05_128x128")
     n0 = qg.qgemm_launch_count()
     qg.GroupwiseWeights(4, 256, 512, p["packed"], p["scales"], T_max=8)
     assert qg.qgemm_launch_count() - n0 == 2            # pack + its ordering kernel

@@ -59,7 +59,8 @@ __host__ __device__ constexpr int hi_bit(int m, int p) { return p < 4 ? 4 * m + 
 // Kernels receive the address of the library's device status word and set it
 // to QGEMM_ERR_TIMEOUT when a bounded wait gives up.
 
-constexpr long long SPIN_LIMIT = 1ll << 22;   // polls of one mbarrier wait (well under seconds)
+constexpr long long SPIN_LIMIT = 1ll << 16;   // tries of one mbarrier wait
+constexpr uint32_t SUSPEND_HINT_NS = 20000;    // at most ~1.3 s per wait in total
 
 // ---------------------------------------------------------------- kernel parameters
 
@@ -104,37 +105,27 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Test of the phase with the given parity.  If the phase is not complete the
+// thread is suspended in hardware until it completes or the hint (in ns)
+// expires, instead of spinning: many waiting warps polling shared memory in a
+// loop slowed every barrier access of the kernel's critical thread.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_HINT_NS) : "memory");
     return ok != 0;
 }
 
 // Bounded wait for the phase with the given parity; false (and the device
-// status set to timeout) if it did not complete within SPIN_LIMIT polls.
+// status set to timeout) if it did not complete within SPIN_LIMIT tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
     for (long long i = 0; i < SPIN_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicExch(status, 7u /* QGEMM_ERR_TIMEOUT */);
     return false;
-}
-
-// Streaming global loads of read-once data: non-coherent path, no L1 allocation.
-__device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ldg_stream_u32(const void *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
 }
 
 // 16-byte asynchronous global -> shared copy (L2 only), committed in groups.

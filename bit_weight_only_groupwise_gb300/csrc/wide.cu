@@ -11,18 +11,23 @@
 //   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, 128 x 64)^T
 //
 // Warp roles (16 warps):
-//   warp 0        producer: 1-D bulk copies of the packed weight units and 2-D
-//                 TMA loads of 128B-swizzled activation tiles into smem rings;
+//   warp 0        weight producer: 1-D bulk copies of the packed units into a
+//                 deep smem ring;
 //   warp 1        allocates tensor memory; one lane issues the MMAs;
+//   warp 2        activation producer: 2-D TMA loads of 128B-swizzled X tiles;
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
 //                 the group (magic-number bf16 decode, exact) and stores them
 //                 into tensor memory as the A operand (tcgen05.st), so shared
-//                 memory bandwidth is left to the B operand;
+//                 memory bandwidth is left to the B operand; two groups per
+//                 iteration overlap their chains, and the row's scale goes to
+//                 the epilogue through a small shared-memory ring;
 //   warps 8..15   epilogue: read P_g from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
 //                 (packed f32x2 FMA), then write Y.
-// Tensor memory: two P buffers of 128 columns (the MMA fills one while the
+// Tensor memory: NP = 2 P buffers of 128 columns (the MMA fills one while the
 // epilogue drains the other) and NA A stages of 32 columns (64 bf16 per row).
+// The two producers run independently so that neither stream waits on the
+// other's ring.
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // to timeout and the CTA winds down.
 #include <cuda.h>
@@ -36,20 +41,28 @@ namespace wide {
 constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
 constexpr int BN = 128;                   // tokens per CTA (MMA N)
 constexpr int NX = 6;                     // activation tile stages (16 KB each)
-constexpr int NW = 4;                     // weight unit stages
-constexpr int NA = 4;                     // A stages in tensor memory
-constexpr int THREADS = 512;
+constexpr int NW = 16;                    // weight unit stages
+constexpr int NA = 8;                     // A stages in tensor memory
+constexpr int NP = 2;                     // P buffers in tensor memory
+constexpr int DQ_WARPS = 4;               // one dequant warp per TMEM lane quarter
+constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
+constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
+constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
+constexpr int SC_RING = 16;               // groups of scales in flight (dequant leads the epilogue by < NA + NP + 3)
+static_assert(SC_RING >= NA + NP + 3, "scale ring shorter than the dequant lead");
 constexpr int X_STAGE = BN * GROUP * 2;   // 16 KB
-constexpr int P_COL = 0;                  // P buffers: columns [0, 256)
-constexpr int A_COL = 256;                // A stages: columns [256, 256 + 32*NA)
+constexpr int P_COL = 0;                  // P buffers: columns [0, 128*NP)
+constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NA)
+static_assert(A_COL + 32 * NA <= 512, "tensor memory budget");
 constexpr int TMEM_COLS = 512;
 
 struct Smem {
     static constexpr int X_OFF = 0;                          // 1024-aligned (128B swizzle atoms)
     static constexpr int W_OFF = X_OFF + NX * X_STAGE;
     static constexpr int BAR_OFF = W_OFF + NW * UNIT5;
-    static constexpr int NBAR = 2 * NX + 2 * NW + 2 * NA + 2 * 2;
-    static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int NBAR = 2 * NX + 2 * NW + 2 * NA + 2 * NP;
+    static constexpr int SC_OFF = BAR_OFF + NBAR * 8;                 // float [SC_RING][BM]
+    static constexpr int TADDR_OFF = SC_OFF + SC_RING * BM * 4;
     static constexpr int BYTES = TADDR_OFF + 16 + 1024;      // + slack to align the base
 };
 
@@ -165,7 +178,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     uint64_t *x_full = bars, *x_empty = x_full + NX;
     uint64_t *w_full = x_empty + NX, *w_empty = w_full + NW;
     uint64_t *a_full = w_empty + NW, *a_empty = a_full + NA;
-    uint64_t *p_full = a_empty + NA, *p_empty = p_full + 2;
+    uint64_t *p_full = a_empty + NA, *p_empty = p_full + NP;
+    float *sc_ring = reinterpret_cast<float *>(smem + Smem::SC_OFF);
     volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
     volatile uint32_t *abort_flag = taddr_slot + 1;
 
@@ -186,9 +200,9 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
-        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }
+        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }   // 4 of the 8 dequant warps read a stage
         for (int i = 0; i < NA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 8); }
+        for (int i = 0; i < NP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], EPI_WARPS); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -203,15 +217,24 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const uint32_t tmem = *taddr_slot;
 
     if (warp == 0) {
-        // ---------------- producer
+        // ---------------- weight producer: packed units, 1-D bulk copies
         if (lane == 0) {
             bool ok = true;
             for (int g = 0; g < G && ok; ++g) {
-                const int wsl = g % NW, xsl = g % NX;
+                const int wsl = g % NW;
                 if (g >= NW) ok = mbar_wait(&w_empty[wsl], ((g / NW) - 1) & 1, args.status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&w_full[wsl], UB);
                 bulk_g2s(ws + wsl * UNIT5, units + (size_t)g * UB, UB, &w_full[wsl]);
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else if (warp == 2) {
+        // ---------------- activation producer: 128B-swizzled X tiles, 2-D TMA
+        if (lane == 0) {
+            bool ok = true;
+            for (int g = 0; g < G && ok; ++g) {
+                const int xsl = g % NX;
                 if (g >= NX) ok = mbar_wait(&x_empty[xsl], ((g / NX) - 1) & 1, args.status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&x_full[xsl], X_STAGE);
@@ -225,108 +248,124 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             bool ok = true;
             const uint32_t idesc = idesc_bf16(BM, BN);
             for (int g = 0; g < G && ok; ++g) {
-                const int asl = g % NA, xsl = g % NX, ps = g & 1;
+                const int asl = g % NA, xsl = g % NX, pb = g % NP;
                 ok = mbar_wait(&a_full[asl], (g / NA) & 1, args.status) &&
                      mbar_wait(&x_full[xsl], (g / NX) & 1, args.status) &&
-                     (g < 2 || mbar_wait(&p_empty[ps], ((g / 2) - 1) & 1, args.status));
+                     (g < NP || mbar_wait(&p_empty[pb], ((g / NP) - 1) & 1, args.status));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t d = tmem + P_COL + ps * BN;
+                const uint32_t d = tmem + P_COL + pb * BN;
                 const uint32_t a = tmem + A_COL + asl * 32;
                 const uint32_t b0 = smem_u32(xs + xsl * X_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < GROUP / 16; ++kk)
                     tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
-                tc_commit(&p_full[ps]);
+                tc_commit(&p_full[pb]);
                 tc_commit(&a_empty[asl]);
                 tc_commit(&x_empty[xsl]);
             }
             if (!ok) *abort_flag = 1;
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- dequant: thread = weight row r of the block
+    } else if (warp >= DQ0 && warp < EPI0) {
+        // ---------------- dequant: thread = weight row r of the block, two
+        // groups per iteration so that their load/decode/store chains overlap
         const int q = warp & 3;                   // TMEM lane quarter
         const int r = q * 32 + lane;
         const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
+        const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
+        const uint32_t tlane = (uint32_t)(q * 32) << 16;
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
-            const int wsl = g % NW, asl = g % NA;
-            ok = mbar_wait(&w_full[wsl], (g / NW) & 1, args.status);
-            if (!ok) break;
-            const uint8_t *u = ws + wsl * UNIT5;
-            uint32_t wd[8];                       // words: (c, 0) k 16c..16c+7, (c, 1) k 16c+8..16c+15
-            uint32_t hw[4];
+        for (int g0 = 0; g0 < G && ok; g0 += 2) {
+            const int ng = G - g0 < 2 ? G - g0 : 2;
+            uint32_t av[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
-                wd[2 * c] = v.x;
-                wd[2 * c + 1] = v.y;
-                hw[c] = codec == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&w_empty[wsl]);
-            // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
-            uint32_t av[32];
+            for (int e = 0; e < 2; ++e) {
+                if (e < ng) {
+                    const int g = g0 + e, wsl = g % NW;
+                    ok = ok && mbar_wait(&w_full[wsl], (g / NW) & 1, args.status);
+                    if (!ok) break;
+                    const uint8_t *u = ws + wsl * UNIT5;
+                    uint32_t wd[8], hw[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
+                        wd[2 * c] = v.x;
+                        wd[2 * c + 1] = v.y;
+                        hw[c] = codec == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
+                    }
+                    // the epilogue of group g reads this row's scale from the ring
+                    sc_ring[(g % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[wsl]);
+                    // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t w = wd[2 * c + h];
-                    uint32_t *o = av + 8 * c + 4 * h;
-                    if (codec == 4) {
-                        o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
-                    } else {
-                        // this row's words in the lane's high word: m = 2*half + h
-                        const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
-                        o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
-                        o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t w = wd[2 * c + h];
+                            uint32_t *o = av[e] + 8 * c + 4 * h;
+                            if (codec == 4) {
+                                o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                            } else {
+                                // this row's words in the lane's high word: m = 2*half + h
+                                const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
+                                o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                                o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                            }
+                        }
                     }
                 }
             }
-            if (g >= NA) ok = mbar_wait(&a_empty[asl], ((g / NA) - 1) & 1, args.status);
             if (!ok) break;
-            tc_fence_after();
-            tc_st32(tmem + ((uint32_t)(q * 32) << 16) + A_COL + asl * 32, av);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (e < ng) {
+                    const int g = g0 + e, asl = g % NA;
+                    if (g >= NA) ok = ok && mbar_wait(&a_empty[asl], ((g / NA) - 1) & 1, args.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    tc_st32(tmem + tlane + A_COL + asl * 32, av[e]);
+                }
+            }
+            if (!ok) break;
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[asl]);
+            if (lane == 0) {
+                for (int e = 0; e < ng; ++e) mbar_arrive(&a_full[(g0 + e) % NA]);
+            }
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp >= 8) {
+    } else if (warp >= EPI0) {
         // ---------------- epilogue: thread = row r, columns [64*hc, 64*hc + 64)
-        const int q = warp & 3, hc = (warp - 8) >> 2;
+        const int q = warp & 3, hc = (warp - EPI0) >> 2;
         const int r = q * 32 + lane;
-        const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
-        const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
         float2 acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
         bool ok = true;
-        uint16_t s_next = *reinterpret_cast<const uint16_t *>(units + soff);
         for (int g = 0; g < G && ok; ++g) {
-            const uint16_t s_bits = s_next;
-            if (g + 1 < G) s_next = *reinterpret_cast<const uint16_t *>(units + (size_t)(g + 1) * UB + soff);
-            const int ps = g & 1;
-            ok = mbar_wait(&p_full[ps], (g / 2) & 1, args.status);
+            const int ps = g % NP;
+            ok = mbar_wait(&p_full[ps], (g / NP) & 1, args.status);
             if (!ok) break;
             tc_fence_after();
+            const float s = sc_ring[(g % SC_RING) * BM + r];
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
-            uint32_t v0[32], v1[32];
-            tc_ld32(base, v0);
-            tc_ld32(base + 32, v1);
+            const float2 s2 = make_float2(s, s);
+            uint32_t v[32];
+            tc_ld32(base, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                acc[j] = ffma2(s2, make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), acc[j]);
+            tc_ld32(base + 32, v);
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_empty[ps]);
-            const float s = __half2float(__ushort_as_half(s_bits));
-            const float2 s2 = make_float2(s, s);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
+                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), acc[16 + j]);
         }
         if (!ok) *abort_flag = 1;
         // ---- write Y[t][n] (consecutive lanes = consecutive rows n)

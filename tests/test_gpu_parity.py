@@ -255,3 +255,20 @@ def test_column_independence_within_tolerance():
         Yref, A = oracle.gemm_parent(p, x[t:t + 1])
         assert_close(Yt, Yref, A)
         assert np.all(np.abs(Yt[0] - Yall[t]) <= 2e-3 * A[0] + 2e-6)
+
+
+@pytest.mark.parametrize("T", [4, 100])
+def test_row_shards_reproduce_the_full_result(T):
+    # the data-parallel split: each shard of rows packed and run on its own
+    # gives exactly its columns of the unsharded result (rows are independent)
+    from bit_weight_only_groupwise_gb300 import sharding
+    N, K = 1000, 512
+    p = synth.weights(12, N, K, 4)
+    X = dev_x(synth.activations(12, T, K, outliers=True))
+    full = y_host(make_weights(p, T_max=T).run(X))
+    parts = []
+    for rank in range(3):
+        codes, scales, start, stop = sharding.shard_inputs(p["packed"], p["scales"], N, 3, rank)
+        W = qg.GroupwiseWeights(4, stop - start, K, codes, scales, T_max=T)
+        parts.append(y_host(W.run(X)))
+    assert np.array_equal(np.concatenate(parts, axis=1), full)

@@ -14,15 +14,8 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
                         cudaStream_t stream);
 cudaError_t launch_fence(cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
-struct WideParent {
-    const uint8_t *packed;
-    float *Y;
-    int N, codec;
-    int cta_begin;
-    int nblocks;
-};
 cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int *launches);
 }  // namespace qg
 
 using namespace qg;
@@ -255,8 +248,9 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
             wp[i].N = plans[i]->N;
             wp[i].codec = plans[i]->codec;
         }
-        if (launch_wide(wp, np, X, T, K, status, stream) != cudaSuccess) return QGEMM_ERR_CUDA;
-        g_launches.fetch_add(1);
+        int launches = 0;
+        if (launch_wide(wp, np, X, T, K, status, stream, &launches) != cudaSuccess) return QGEMM_ERR_CUDA;
+        g_launches.fetch_add(launches);
         return QGEMM_OK;
     }
     bool pdl = true;

@@ -82,6 +82,15 @@ struct SkinnyArgs {
     unsigned int *status;    // device status word
 };
 
+// The wide route's grid has ceil(N/128) x ceil(T/128) CTAs per parent.
+struct WideParent {
+    const uint8_t *packed;   // units of this parent
+    float *Y;                // [T][N]
+    int N, codec;
+    int cta_begin;           // first CTA of this parent in its launch
+    int nblocks;             // 128-row blocks
+};
+
 // ---------------------------------------------------------------- PTX wrappers
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -119,13 +128,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity; false (and the device
-// status set to timeout) if it did not complete within SPIN_LIMIT tries.
+// status set to timeout) if it did not complete within SPIN_LIMIT tries.  A
+// phase that has already completed is seen by the non-blocking test, which
+// is cheaper than the suspending form.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    if (mbar_test(bar, parity)) return true;
     for (long long i = 0; i < SPIN_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicExch(status, 7u /* QGEMM_ERR_TIMEOUT */);
     return false;
+}
+
+// One lane of a converged warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+    return p != 0;
+}
+
+// Bounded wait by every lane of a converged warp; the result is the same in
+// all lanes (false if any lane gave up), so the warp stays converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
 // 16-byte asynchronous global -> shared copy (L2 only), committed in groups.

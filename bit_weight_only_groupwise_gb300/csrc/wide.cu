@@ -10,26 +10,32 @@
 //   D[128 rows x 128 tokens] = sum over 64-column groups g of s[:, g] * P_g,
 //   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, 128 x 64)^T
 //
-// Warp roles (16 warps):
+// Warp roles (16 warps; every single-issuer role is a converged warp whose
+// elected lane issues, and every wait is taken by the whole warp):
 //   warp 0        weight producer: 1-D bulk copies of the packed units into a
 //                 deep smem ring;
-//   warp 1        allocates tensor memory; one lane issues the MMAs;
+//   warp 1        allocates tensor memory and issues the MMAs;
 //   warp 2        activation producer: 2-D TMA loads of 128B-swizzled X tiles;
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
 //                 the group (magic-number bf16 decode, exact) and stores them
 //                 into tensor memory as the A operand (tcgen05.st), so shared
-//                 memory bandwidth is left to the B operand; two groups per
-//                 iteration overlap their chains, and the row's scale goes to
-//                 the epilogue through a small shared-memory ring;
+//                 memory bandwidth is left to the B operand; the row's scale
+//                 goes to the epilogue through a small shared-memory ring;
 //   warps 8..15   epilogue: read P_g from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
 //                 (packed f32x2 FMA), then write Y.
 // Tensor memory: NP = 2 P buffers of 128 columns (the MMA fills one while the
-// epilogue drains the other) and NA A stages of 32 columns (64 bf16 per row).
-// The two producers run independently so that neither stream waits on the
-// other's ring.
+// epilogue drains the other) and NS A stages of 32 columns (64 bf16 per row).
+// Synchronisation per group g (stage s = g mod NS):
+//   go[s]     completes when A_g is in tensor memory (4 dequant arrivals),
+//             X_g has landed (TMA transaction bytes + 1 arrival) and the P
+//             buffer of g is drained (8 epilogue arrivals after group g - NP):
+//             the MMA warp waits on this one barrier per group;
+//   freed[s]  MMA commit: A and X stage s may be overwritten;
+//   p_full    MMA commit: P_g is complete.
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
-// to timeout and the CTA winds down.
+// to timeout and the CTA winds down (after a bounded pause that lets copies
+// and MMAs already issued land before tensor memory is released).
 #include <cuda.h>
 
 #include "qgemm_internal.cuh"
@@ -40,41 +46,36 @@ namespace wide {
 
 constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
 constexpr int BN = 128;                   // tokens per CTA (MMA N)
-constexpr int NX = 6;                     // activation tile stages (16 KB each)
+constexpr int NS = 8;                     // activation / A stages (one ring index)
 constexpr int NW = 16;                    // weight unit stages
-constexpr int NA = 8;                     // A stages in tensor memory
 constexpr int NP = 2;                     // P buffers in tensor memory
 constexpr int DQ_WARPS = 4;               // one dequant warp per TMEM lane quarter
 constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
 constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
 constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
-constexpr int SC_RING = 16;               // groups of scales in flight (dequant leads the epilogue by < NA + NP + 3)
-static_assert(SC_RING >= NA + NP + 3, "scale ring shorter than the dequant lead");
+constexpr int GO_COUNT = DQ_WARPS + 1 + EPI_WARPS;
+constexpr int SC_RING = 16;               // groups of scales in flight
+// the dequant stores the scale of group g once the epilogue has finished group g - NS - NP - 1
+static_assert(SC_RING >= NS + NP + 2, "scale ring shorter than the dequant lead");
+static_assert(NS > NP, "go barrier phases need more stages than P buffers");
 constexpr int X_STAGE = BN * GROUP * 2;   // 16 KB
 constexpr int P_COL = 0;                  // P buffers: columns [0, 128*NP)
-constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NA)
-static_assert(A_COL + 32 * NA <= 512, "tensor memory budget");
+constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NS)
+static_assert(A_COL + 32 * NS <= 512, "tensor memory budget");
 constexpr int TMEM_COLS = 512;
 
 struct Smem {
     static constexpr int X_OFF = 0;                          // 1024-aligned (128B swizzle atoms)
-    static constexpr int W_OFF = X_OFF + NX * X_STAGE;
+    static constexpr int W_OFF = X_OFF + NS * X_STAGE;
     static constexpr int BAR_OFF = W_OFF + NW * UNIT5;
-    static constexpr int NBAR = 2 * NX + 2 * NW + 2 * NA + 2 * NP;
+    static constexpr int NBAR = 2 * NW + 2 * NS + NP;
     static constexpr int SC_OFF = BAR_OFF + NBAR * 8;                 // float [SC_RING][BM]
     static constexpr int TADDR_OFF = SC_OFF + SC_RING * BM * 4;
     static constexpr int BYTES = TADDR_OFF + 16 + 1024;      // + slack to align the base
 };
+static_assert(Smem::BYTES <= 227 * 1024, "shared memory budget");
 
 }  // namespace wide
-
-struct WideParent {
-    const uint8_t *packed;
-    float *Y;
-    int N, codec;
-    int cta_begin;        // first CTA of this parent
-    int nblocks;          // 128-row blocks
-};
 
 struct WideArgs {
     WideParent p[MAX_PARENTS];
@@ -167,6 +168,9 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 // ---------------------------------------------------------------- the kernel
 
+// CODEC: the codec of every parent of the launch (4 or 5); a launch whose
+// parents mix codecs is split into one launch per codec by the host.
+template <int CODEC>
 __global__ void __launch_bounds__(wide::THREADS, 1)
     wide_kernel(const __grid_constant__ WideArgs args, const __grid_constant__ CUtensorMap xmap) {
     using namespace wide;
@@ -175,10 +179,9 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     uint8_t *xs = smem + Smem::X_OFF;
     uint8_t *ws = smem + Smem::W_OFF;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::BAR_OFF);
-    uint64_t *x_full = bars, *x_empty = x_full + NX;
-    uint64_t *w_full = x_empty + NX, *w_empty = w_full + NW;
-    uint64_t *a_full = w_empty + NW, *a_empty = a_full + NA;
-    uint64_t *p_full = a_empty + NA, *p_empty = p_full + NP;
+    uint64_t *w_full = bars, *w_empty = w_full + NW;
+    uint64_t *go = w_empty + NW, *freed = go + NS;
+    uint64_t *p_full = freed + NS;
     float *sc_ring = reinterpret_cast<float *>(smem + Smem::SC_OFF);
     volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
     volatile uint32_t *abort_flag = taddr_slot + 1;
@@ -192,17 +195,16 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const int local = blockIdx.x - P.cta_begin;
     const int blk = local / args.ntt, tt = local % args.ntt;
     const int G = args.G, T = args.T;
-    const int codec = P.codec;
-    const int UB = unit_bytes(codec);
+    constexpr int codec = CODEC;
+    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
     const uint8_t *units = P.packed + (size_t)blk * G * UB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
-        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], 4); }   // 4 of the 8 dequant warps read a stage
-        for (int i = 0; i < NA; ++i) { mbar_init(&a_full[i], 4); mbar_init(&a_empty[i], 1); }
-        for (int i = 0; i < NP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], EPI_WARPS); }
+        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], DQ_WARPS); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&go[i], GO_COUNT); mbar_init(&freed[i], 1); }
+        for (int i = 0; i < NP; ++i) mbar_init(&p_full[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -218,136 +220,116 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
 
     if (warp == 0) {
         // ---------------- weight producer: packed units, 1-D bulk copies
-        if (lane == 0) {
-            bool ok = true;
-            for (int g = 0; g < G && ok; ++g) {
-                const int wsl = g % NW;
-                if (g >= NW) ok = mbar_wait(&w_empty[wsl], ((g / NW) - 1) & 1, args.status);
-                if (!ok) break;
+        bool ok = true;
+        for (int g = 0; g < G; ++g) {
+            const int wsl = g % NW;
+            if (g >= NW && !(ok = mbar_wait_warp(&w_empty[wsl], ((g / NW) - 1) & 1, args.status))) break;
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&w_full[wsl], UB);
                 bulk_g2s(ws + wsl * UNIT5, units + (size_t)g * UB, UB, &w_full[wsl]);
             }
-            if (!ok) *abort_flag = 1;
+            __syncwarp();
         }
+        if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp == 2) {
         // ---------------- activation producer: 128B-swizzled X tiles, 2-D TMA
-        if (lane == 0) {
-            bool ok = true;
-            for (int g = 0; g < G && ok; ++g) {
-                const int xsl = g % NX;
-                if (g >= NX) ok = mbar_wait(&x_empty[xsl], ((g / NX) - 1) & 1, args.status);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&x_full[xsl], X_STAGE);
-                tma_load_2d(xs + xsl * X_STAGE, &xmap, g * GROUP, tt * BN, &x_full[xsl]);
+        bool ok = true;
+        for (int g = 0; g < G; ++g) {
+            const int s = g % NS;
+            if (g >= NS && !(ok = mbar_wait_warp(&freed[s], ((g / NS) - 1) & 1, args.status))) break;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&go[s], X_STAGE);
+                tma_load_2d(xs + s * X_STAGE, &xmap, g * GROUP, tt * BN, &go[s]);
             }
-            if (!ok) *abort_flag = 1;
+            __syncwarp();
         }
+        if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp == 1) {
         // ---------------- MMA issuer
-        if (lane == 0) {
-            bool ok = true;
-            const uint32_t idesc = idesc_bf16(BM, BN);
-            for (int g = 0; g < G && ok; ++g) {
-                const int asl = g % NA, xsl = g % NX, pb = g % NP;
-                ok = mbar_wait(&a_full[asl], (g / NA) & 1, args.status) &&
-                     mbar_wait(&x_full[xsl], (g / NX) & 1, args.status) &&
-                     (g < NP || mbar_wait(&p_empty[pb], ((g / NP) - 1) & 1, args.status));
-                if (!ok) break;
-                tc_fence_after();
+        bool ok = true;
+        const uint32_t idesc = idesc_bf16(BM, BN);
+        for (int g = 0; g < G; ++g) {
+            const int s = g % NS, pb = g % NP;
+            if (!(ok = mbar_wait_warp(&go[s], (g / NS) & 1, args.status))) break;
+            tc_fence_after();
+            if (elect_one()) {
                 const uint32_t d = tmem + P_COL + pb * BN;
-                const uint32_t a = tmem + A_COL + asl * 32;
-                const uint32_t b0 = smem_u32(xs + xsl * X_STAGE);
+                const uint32_t a = tmem + A_COL + s * 32;
+                const uint32_t b0 = smem_u32(xs + s * X_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < GROUP / 16; ++kk)
                     tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
                 tc_commit(&p_full[pb]);
-                tc_commit(&a_empty[asl]);
-                tc_commit(&x_empty[xsl]);
+                tc_commit(&freed[s]);
             }
-            if (!ok) *abort_flag = 1;
+            __syncwarp();
         }
+        if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp >= DQ0 && warp < EPI0) {
-        // ---------------- dequant: thread = weight row r of the block, two
-        // groups per iteration so that their load/decode/store chains overlap
+        // ---------------- dequant: thread = weight row r of the block
         const int q = warp & 3;                   // TMEM lane quarter
         const int r = q * 32 + lane;
         const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
         const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         bool ok = true;
-        for (int g0 = 0; g0 < G && ok; g0 += 2) {
-            const int ng = G - g0 < 2 ? G - g0 : 2;
-            uint32_t av[2][32];
+        for (int g = 0; g < G; ++g) {
+            const int wsl = g % NW, s = g % NS;
+            if (!(ok = mbar_wait_warp(&w_full[wsl], (g / NW) & 1, args.status))) break;
+            const uint8_t *u = ws + wsl * UNIT5;
+            uint32_t wd[8], hw[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (e < ng) {
-                    const int g = g0 + e, wsl = g % NW;
-                    ok = ok && mbar_wait(&w_full[wsl], (g / NW) & 1, args.status);
-                    if (!ok) break;
-                    const uint8_t *u = ws + wsl * UNIT5;
-                    uint32_t wd[8], hw[4];
+            for (int c = 0; c < 4; ++c) {
+                const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
+                wd[2 * c] = v.x;
+                wd[2 * c + 1] = v.y;
+                hw[c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
+            }
+            // the epilogue of group g reads this row's scale from the ring
+            sc_ring[(g % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
+            // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
+            uint32_t av[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
-                        wd[2 * c] = v.x;
-                        wd[2 * c + 1] = v.y;
-                        hw[c] = codec == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
-                    }
-                    // the epilogue of group g reads this row's scale from the ring
-                    sc_ring[(g % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&w_empty[wsl]);
-                    // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t w = wd[2 * c + h];
-                            uint32_t *o = av[e] + 8 * c + 4 * h;
-                            if (codec == 4) {
-                                o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
-                            } else {
-                                // this row's words in the lane's high word: m = 2*half + h
-                                const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
-                                o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
-                                o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
-                            }
-                        }
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t w = wd[2 * c + h];
+                    uint32_t *o = av + 8 * c + 4 * h;
+                    if (CODEC == 4) {
+                        o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                    } else {
+                        // this row's words in the lane's high word: m = 2*half + h
+                        const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
+                        o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                        o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
                     }
                 }
             }
-            if (!ok) break;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (e < ng) {
-                    const int g = g0 + e, asl = g % NA;
-                    if (g >= NA) ok = ok && mbar_wait(&a_empty[asl], ((g / NA) - 1) & 1, args.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    tc_st32(tmem + tlane + A_COL + asl * 32, av[e]);
-                }
-            }
-            if (!ok) break;
+            if (g >= NS && !(ok = mbar_wait_warp(&freed[s], ((g / NS) - 1) & 1, args.status))) break;
+            tc_fence_after();
+            tc_st32(tmem + tlane + A_COL + s * 32, av);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                for (int e = 0; e < ng; ++e) mbar_arrive(&a_full[(g0 + e) % NA]);
-            }
+            if (lane == 0) mbar_arrive(&go[s]);
         }
-        if (!ok) *abort_flag = 1;
+        if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp >= EPI0) {
         // ---------------- epilogue: thread = row r, columns [64*hc, 64*hc + 64)
         const int q = warp & 3, hc = (warp - EPI0) >> 2;
         const int r = q * 32 + lane;
+        // the first NP groups find their P buffer empty
+        if (lane == 0)
+            for (int g = 0; g < NP && g < G; ++g) mbar_arrive(&go[g]);
         float2 acc[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
         bool ok = true;
-        for (int g = 0; g < G && ok; ++g) {
+        for (int g = 0; g < G; ++g) {
             const int ps = g % NP;
-            ok = mbar_wait(&p_full[ps], (g / NP) & 1, args.status);
-            if (!ok) break;
+            if (!(ok = mbar_wait_warp(&p_full[ps], (g / NP) & 1, args.status))) break;
             tc_fence_after();
             const float s = sc_ring[(g % SC_RING) * BM + r];
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
@@ -362,12 +344,13 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_empty[ps]);
+            // P buffer ps is free for group g + NP
+            if (lane == 0 && g + NP < G) mbar_arrive(&go[(g + NP) % NS]);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), acc[16 + j]);
         }
-        if (!ok) *abort_flag = 1;
+        if (!ok && lane == 0) *abort_flag = 1;
         // ---- write Y[t][n] (consecutive lanes = consecutive rows n)
         const int n = blk * BM + r;
         if (ok && n < P.N) {
@@ -384,6 +367,13 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     // ---- every role is done with tensor memory: release it
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        // a wait gave up: copies and MMAs already issued finish within
+        // microseconds; give them a bounded pause before the memory they
+        // write is released
+        for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS) : "memory");
@@ -429,38 +419,53 @@ static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K) {
 
 int wide_tile_tokens() { return wide::BN; }
 
-cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
-                        cudaStream_t stream) {
+template <int CODEC>
+static cudaError_t launch_codec(const WideParent *parents, int np, const CUtensorMap &xmap, int T, int K,
+                                unsigned int *status, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::Smem::BYTES);
+        e = cudaFuncSetAttribute(wide_kernel<CODEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::Smem::BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    CUtensorMap xmap;
-    if ((e = make_xmap(&xmap, X, T, K)) != cudaSuccess) return e;
     WideArgs a;
     memset(&a, 0, sizeof a);
     const int ntt = (T + wide::BN - 1) / wide::BN;
     int grid = 0;
     for (int i = 0; i < np; ++i) {
-        a.p[i] = parents[i];
-        a.p[i].cta_begin = grid;
-        a.p[i].nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
-        grid += a.p[i].nblocks * ntt;
+        if (parents[i].codec != CODEC) continue;
+        WideParent &d = a.p[a.nparents++];
+        d = parents[i];
+        d.cta_begin = grid;
+        d.nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
+        grid += d.nblocks * ntt;
     }
-    a.nparents = np;
+    if (grid == 0) return cudaSuccess;
     a.T = T;
     a.K = K;
     a.G = K / GROUP;
     a.ntt = ntt;
     a.status = status;
-    wide_kernel<<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
+    wide_kernel<CODEC><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
     return cudaGetLastError();
+}
+
+// Parents of both codecs in one call become one launch per codec.
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
+                        cudaStream_t stream, int *launches) {
+    CUtensorMap xmap;
+    cudaError_t e = make_xmap(&xmap, X, T, K);
+    if (e != cudaSuccess) return e;
+    int n4 = 0, n5 = 0;
+    for (int i = 0; i < np; ++i) (parents[i].codec == 4 ? n4 : n5)++;
+    if (n4 && (e = launch_codec<4>(parents, np, xmap, T, K, status, stream)) != cudaSuccess) return e;
+    if (n5 && (e = launch_codec<5>(parents, np, xmap, T, K, status, stream)) != cudaSuccess) return e;
+    *launches = (n4 > 0) + (n5 > 0);
+    return cudaSuccess;
 }
 
 }  // namespace qg

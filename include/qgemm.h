@@ -132,8 +132,9 @@ qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_
  * single launch, as the two-parent projections of "ninfer-3080
  * docs/performance.md" (A8 prefill routes section: two parents over one
  * activation share its preparation).  All plans must have the same K and
- * T <= each plan's T_max; codecs may differ.  Ys[i] receives parent i's
- * [T][N_i] result.  1 <= n_parents <= 4.
+ * T <= each plan's T_max; codecs may differ (on the tensor-core route, used
+ * from T = 33 up, parents of different codecs take one launch per codec).
+ * Ys[i] receives parent i's [T][N_i] result.  1 <= n_parents <= 4.
  */
 qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
                              float *const *Ys, qgemm_stream_t stream);

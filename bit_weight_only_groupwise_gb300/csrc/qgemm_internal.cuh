@@ -158,6 +158,16 @@ __device__ __forceinline__ bool elect_one() {
     return p != 0;
 }
 
+// Bounded wait for two phases; the two non-blocking tests are issued together
+// so that two completed phases cost one round trip.
+__device__ __forceinline__ bool mbar_wait2(uint64_t *bar0, uint32_t parity0, uint64_t *bar1, uint32_t parity1,
+                                           unsigned int *status) {
+    const bool r0 = mbar_test(bar0, parity0);
+    const bool r1 = mbar_test(bar1, parity1);
+    if (r0 && r1) return true;
+    return (r0 || mbar_wait(bar0, parity0, status)) && (r1 || mbar_wait(bar1, parity1, status));
+}
+
 // Bounded wait by every lane of a converged warp; the result is the same in
 // all lanes (false if any lane gave up), so the warp stays converged.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, unsigned int *status) {

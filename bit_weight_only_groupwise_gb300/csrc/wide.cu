@@ -14,7 +14,8 @@
 // elected lane issues, and every wait is taken by the whole warp):
 //   warp 0        weight producer: 1-D bulk copies of the packed units into a
 //                 deep smem ring;
-//   warp 1        allocates tensor memory and issues the MMAs;
+//   warp 1        allocates tensor memory and issues the MMAs of even
+//                 groups; warp 3 issues those of odd groups;
 //   warp 2        activation producer: 2-D TMA loads of 128B-swizzled X tiles;
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
 //                 the group (magic-number bf16 decode, exact) and stores them
@@ -31,8 +32,10 @@
 //             X_g has landed (TMA transaction bytes + 1 arrival) and the P
 //             buffer of g is drained (8 epilogue arrivals after group g - NP):
 //             the MMA warp waits on this one barrier per group;
-//   freed[s]  MMA commit: A and X stage s may be overwritten;
-//   p_full    MMA commit: P_g is complete.
+//   done[s]   the MMA commit of group g: P_g is complete (the epilogue waits
+//             on it) and A and X stage s may be overwritten (the dequant and
+//             the activation producer wait on it for group g + NS); one
+//             commit per group, as every MMA issue costs the issuing thread.
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // to timeout and the CTA winds down (after a bounded pause that lets copies
 // and MMAs already issued land before tensor memory is released).
@@ -47,7 +50,7 @@ namespace wide {
 constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
 constexpr int BN = 128;                   // tokens per CTA (MMA N)
 constexpr int NS = 8;                     // activation / A stages (one ring index)
-constexpr int NW = 16;                    // weight unit stages
+constexpr int NWP = 8;                    // weight stages, each a pair of consecutive groups' units
 constexpr int NP = 2;                     // P buffers in tensor memory
 constexpr int DQ_WARPS = 4;               // one dequant warp per TMEM lane quarter
 constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
@@ -67,8 +70,8 @@ constexpr int TMEM_COLS = 512;
 struct Smem {
     static constexpr int X_OFF = 0;                          // 1024-aligned (128B swizzle atoms)
     static constexpr int W_OFF = X_OFF + NS * X_STAGE;
-    static constexpr int BAR_OFF = W_OFF + NW * UNIT5;
-    static constexpr int NBAR = 2 * NW + 2 * NS + NP;
+    static constexpr int BAR_OFF = W_OFF + NWP * 2 * UNIT5;
+    static constexpr int NBAR = 2 * NWP + 2 * NS;
     static constexpr int SC_OFF = BAR_OFF + NBAR * 8;                 // float [SC_RING][BM]
     static constexpr int TADDR_OFF = SC_OFF + SC_RING * BM * 4;
     static constexpr int BYTES = TADDR_OFF + 16 + 1024;      // + slack to align the base
@@ -131,6 +134,18 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
 }
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties registers filled by tcgen05.ld to a point after tcgen05.wait::ld: code
+// that reads them depends on this statement's outputs, so the compiler cannot
+// move it above the wait.
+__device__ __forceinline__ void tc_regs_ready(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                   "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]),
+                   "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 2-D tiled TMA load of box {64 columns, 128 rows} at (x, y) into smem.
@@ -179,9 +194,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     uint8_t *xs = smem + Smem::X_OFF;
     uint8_t *ws = smem + Smem::W_OFF;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::BAR_OFF);
-    uint64_t *w_full = bars, *w_empty = w_full + NW;
-    uint64_t *go = w_empty + NW, *freed = go + NS;
-    uint64_t *p_full = freed + NS;
+    uint64_t *w_full = bars, *w_empty = w_full + NWP;
+    uint64_t *go = w_empty + NWP, *done = go + NS;
     float *sc_ring = reinterpret_cast<float *>(smem + Smem::SC_OFF);
     volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
     volatile uint32_t *abort_flag = taddr_slot + 1;
@@ -202,9 +216,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NW; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], DQ_WARPS); }
-        for (int i = 0; i < NS; ++i) { mbar_init(&go[i], GO_COUNT); mbar_init(&freed[i], 1); }
-        for (int i = 0; i < NP; ++i) mbar_init(&p_full[i], 1);
+        for (int i = 0; i < NWP; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], DQ_WARPS); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&go[i], GO_COUNT); mbar_init(&done[i], 1); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -219,14 +232,16 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const uint32_t tmem = *taddr_slot;
 
     if (warp == 0) {
-        // ---------------- weight producer: packed units, 1-D bulk copies
+        // ---------------- weight producer: the units of groups (2j, 2j+1) in one
+        // 1-D bulk copy (a row block's units are consecutive in memory)
         bool ok = true;
-        for (int g = 0; g < G; ++g) {
-            const int wsl = g % NW;
-            if (g >= NW && !(ok = mbar_wait_warp(&w_empty[wsl], ((g / NW) - 1) & 1, args.status))) break;
+        for (int j = 0; j < (G + 1) / 2; ++j) {
+            const int wsl = j % NWP;
+            const uint32_t bytes = (2 * j + 1 < G ? 2 : 1) * UB;
+            if (j >= NWP && !(ok = mbar_wait_warp(&w_empty[wsl], ((j / NWP) - 1) & 1, args.status))) break;
             if (elect_one()) {
-                mbar_arrive_expect_tx(&w_full[wsl], UB);
-                bulk_g2s(ws + wsl * UNIT5, units + (size_t)g * UB, UB, &w_full[wsl]);
+                mbar_arrive_expect_tx(&w_full[wsl], bytes);
+                bulk_g2s(ws + wsl * 2 * UNIT5, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
             }
             __syncwarp();
         }
@@ -236,7 +251,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         bool ok = true;
         for (int g = 0; g < G; ++g) {
             const int s = g % NS;
-            if (g >= NS && !(ok = mbar_wait_warp(&freed[s], ((g / NS) - 1) & 1, args.status))) break;
+            if (g >= NS && !(ok = mbar_wait_warp(&done[s], ((g / NS) - 1) & 1, args.status))) break;
             if (elect_one()) {
                 mbar_arrive_expect_tx(&go[s], X_STAGE);
                 tma_load_2d(xs + s * X_STAGE, &xmap, g * GROUP, tt * BN, &go[s]);
@@ -244,76 +259,108 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             __syncwarp();
         }
         if (!ok && lane == 0) *abort_flag = 1;
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ---------------- MMA issuers: warp 1 even groups, warp 3 odd groups.
+        // Issuing a tensor-core instruction occupies the issuing warp's
+        // scheduler for tens of cycles; two issuers on two schedulers halve
+        // what the epilogue and dequant warps sharing them lose, and
+        // consecutive groups' MMA chains (different P buffers) interleave.
         bool ok = true;
         const uint32_t idesc = idesc_bf16(BM, BN);
-        for (int g = 0; g < G; ++g) {
+        for (int g = warp >> 1; g < G; g += 2) {
             const int s = g % NS, pb = g % NP;
             if (!(ok = mbar_wait_warp(&go[s], (g / NS) & 1, args.status))) break;
             tc_fence_after();
-            if (elect_one()) {
-                const uint32_t d = tmem + P_COL + pb * BN;
-                const uint32_t a = tmem + A_COL + s * 32;
-                const uint32_t b0 = smem_u32(xs + s * X_STAGE);
+            const uint32_t d = tmem + P_COL + pb * BN;
+            const uint32_t a = tmem + A_COL + s * 32;
+            const uint32_t b0 = smem_u32(xs + s * X_STAGE);
+            // one elected lane per instruction: measured cheaper to issue than
+            // one elected block of four
 #pragma unroll
-                for (int kk = 0; kk < GROUP / 16; ++kk)
-                    tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
-                tc_commit(&p_full[pb]);
-                tc_commit(&freed[s]);
-            }
+            for (int kk = 0; kk < GROUP / 16; ++kk)
+                if (elect_one()) tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
+            if (elect_one()) tc_commit(&done[s]);
             __syncwarp();
         }
         if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp >= DQ0 && warp < EPI0) {
-        // ---------------- dequant: thread = weight row r of the block
+        // ---------------- dequant: thread = weight row r of the block; groups
+        // (2j, 2j+1) per iteration, so that one weight wait, one stage wait
+        // and one tensor-memory store wait serve two groups and the two
+        // decodes overlap
         const int q = warp & 3;                   // TMEM lane quarter
         const int r = q * 32 + lane;
         const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
         const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         bool ok = true;
-        for (int g = 0; g < G; ++g) {
-            const int wsl = g % NW, s = g % NS;
-            if (!(ok = mbar_wait_warp(&w_full[wsl], (g / NW) & 1, args.status))) break;
-            const uint8_t *u = ws + wsl * UNIT5;
-            uint32_t wd[8], hw[4];
+        for (int j = 0; j < (G + 1) / 2; ++j) {
+            const int g0 = 2 * j;
+            const bool two = g0 + 1 < G;
+            const int wsl = j % NWP;
+            if (!(ok = mbar_wait_warp(&w_full[wsl], (j / NWP) & 1, args.status))) break;
+            uint32_t wd[2][8], hw[2][4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
-                wd[2 * c] = v.x;
-                wd[2 * c + 1] = v.y;
-                hw[c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
+            for (int e = 0; e < 2; ++e) {
+                const uint8_t *u = ws + wsl * 2 * UNIT5 + e * UB;
+                if (e == 0 || two) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
+                        wd[e][2 * c] = v.x;
+                        wd[e][2 * c + 1] = v.y;
+                        hw[e][c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
+                    }
+                    // the epilogue of group g0 + e reads this row's scale from the ring
+                    sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) { wd[e][2 * c] = wd[e][2 * c + 1] = 0u; hw[e][c] = 0u; }
+                }
             }
-            // the epilogue of group g reads this row's scale from the ring
-            sc_ring[(g % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[wsl]);
-            // decode to 32 bf16x2 words in natural k order: word j = (k 2j, 2j+1)
-            uint32_t av[32];
+            // decode to 32 bf16x2 words per group in natural k order: word m = (k 2m, 2m+1)
+            uint32_t av[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int e = 0; e < 2; ++e) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t w = wd[2 * c + h];
-                    uint32_t *o = av + 8 * c + 4 * h;
-                    if (CODEC == 4) {
-                        o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
-                    } else {
-                        // this row's words in the lane's high word: m = 2*half + h
-                        const uint32_t hh = hw[c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
-                        o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
-                        o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t w = wd[e][2 * c + h];
+                        uint32_t *o = av[e] + 8 * c + 4 * h;
+                        if (CODEC == 4) {
+                            o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                        } else {
+                            // this row's words in the lane's high word: m = 2*half + h
+                            const uint32_t hh = hw[e][c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
+                            o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                            o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                        }
                     }
                 }
             }
-            if (g >= NS && !(ok = mbar_wait_warp(&freed[s], ((g / NS) - 1) & 1, args.status))) break;
+            // the A stages of both groups are free once the MMAs of groups
+            // g0 - NS and g0 + 1 - NS have completed
+            if (two && g0 + 1 >= NS) {
+                // (g0 >= NS too: NS is even)
+                ok = __all_sync(0xffffffffu, mbar_wait2(&done[g0 % NS], ((g0 / NS) - 1) & 1, &done[(g0 + 1) % NS],
+                                                        (((g0 + 1) / NS) - 1) & 1, args.status));
+            } else if (g0 >= NS) {
+                ok = mbar_wait_warp(&done[g0 % NS], ((g0 / NS) - 1) & 1, args.status);
+            }
+            if (!ok) break;
             tc_fence_after();
-            tc_st32(tmem + tlane + A_COL + s * 32, av);
+            tc_st32(tmem + tlane + A_COL + (g0 % NS) * 32, av[0]);
+            if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NS) * 32, av[1]);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&go[s]);
+            if (lane == 0) {
+                mbar_arrive(&go[g0 % NS]);
+                if (two) mbar_arrive(&go[(g0 + 1) % NS]);
+            }
         }
         if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp >= EPI0) {
@@ -329,26 +376,30 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         bool ok = true;
         for (int g = 0; g < G; ++g) {
             const int ps = g % NP;
-            if (!(ok = mbar_wait_warp(&p_full[ps], (g / NP) & 1, args.status))) break;
+            if (!(ok = mbar_wait_warp(&done[g % NS], (g / NS) & 1, args.status))) break;
             tc_fence_after();
             const float s = sc_ring[(g % SC_RING) * BM + r];
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
-            const float2 s2 = make_float2(s, s);
-            uint32_t v[32];
-            tc_ld32(base, v);
+            // both loads in flight before one wait: the P buffer is released one
+            // load latency after it filled
+            uint32_t v0[32], v1[32];
+            tc_ld32(base, v0);
+            tc_ld32(base + 32, v1);
             tc_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                acc[j] = ffma2(s2, make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), acc[j]);
-            tc_ld32(base + 32, v);
-            tc_wait_ld();
+            tc_regs_ready(v0);
+            tc_regs_ready(v1);
             tc_fence_before();
             __syncwarp();
             // P buffer ps is free for group g + NP
             if (lane == 0 && g + NP < G) mbar_arrive(&go[(g + NP) % NS]);
+            // packed f32x2 FMAs: half the instructions of scalar ones
+            const float2 s2 = make_float2(s, s);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), acc[16 + j]);
+                acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
         }
         if (!ok && lane == 0) *abort_flag = 1;
         // ---- write Y[t][n] (consecutive lanes = consecutive rows n)

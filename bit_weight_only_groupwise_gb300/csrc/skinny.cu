@@ -7,34 +7,35 @@
 // to be kernel ramp-up and drain; the route boundaries section notes that
 // cold weight streaming is the production regime).  The design:
 //
-// * grid: one CTA per 16-row tile of the weight matrix; its warps split K
-//   (warp kw takes groups kw, kw+KW, ...).  Each warp streams its groups
-//   through a private shared-memory ring: every lane copies, with 16-byte
-//   asynchronous copies, exactly the 16-byte code chunk it will decode (512
-//   contiguous bytes per warp and group), so the bytes in flight cost no
-//   registers and no cross-warp synchronisation.  Measured on this path, this
-//   beat register double-buffering (whose register cost capped occupancy and
-//   bytes in flight) and a bulk-copy ring fed by one producer thread.  A CTA
-//   owns whole output rows and leaves as soon as it is done, so no CTA waits
-//   on another;
+// * grid: one CTA per 16-row tile of the weight matrix; its warps split K.
+//   Two kernels share this scheme.  Where K / 64 is a multiple of 8 (the
+//   shapes of the pages' models), each warp owns 8 consecutive groups and
+//   copies all of them into shared memory at once, with 16-byte asynchronous
+//   copies of exactly the 16-byte code chunk each lane will decode (512
+//   contiguous bytes per warp and group), so the group loop is straight-line
+//   code with immediate offsets and the codec is resolved once per CTA.
+//   Otherwise warp kw takes groups kw, kw+KW, ... through a private ring of 8
+//   stages.  Both keep the bytes in flight out of registers and need no
+//   cross-warp synchronisation until the end; a CTA owns whole output rows and
+//   leaves as soon as it is done, so no CTA waits on another;
 // * the warps decode their lane's 16 codes per row in registers
 //   (magic-number bf16 decode) and run bf16 m16n8k16 tensor-core MMAs against
 //   the activation fragments, whose k order is permuted the same way as the
 //   codes (any permutation inside a group is valid when A and B agree -- the
-//   small-T kernels section's permuted k order); the activation lines of the
-//   groups in the ring are prefetched into L1;
+//   small-T kernels section's permuted k order);
 // * each 64-column group's fp32 partial is multiplied by its fp16 scale and
 //   added to the fp32 accumulator (the per-group rescale of the token-tile
 //   section's ablation): scale * code is never rounded;
 // * the K split inside the CTA is combined in shared memory in warp order --
 //   deterministic, no workspace, no atomics;
 // * programmatic dependent launch: the weights do not depend on the previous
-//   kernel in the stream, so each warp fills its ring before
-//   griddepcontrol.wait, and a CTA lets the next kernel launch once its own
-//   weights have arrived: back-to-back calls overlap their ramp and drain
+//   kernel in the stream, so each warp issues its weight copies before
+//   griddepcontrol.wait, and back-to-back calls overlap their ramp and drain
 //   (the pages name ramp and drain at kernel boundaries as what is left at
-//   one stream).  Triggering at kernel start instead let a cascade of later
-//   kernels flood memory with prefetches and measured slower.
+//   one stream).  Where the next kernel may start is measured per kernel:
+//   see the trigger placements below.
+#include <utility>
+
 #include "qgemm_internal.cuh"
 
 namespace qg {
@@ -234,6 +235,227 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
         for (int q = 1; q < KW; ++q) v += red[(q * T8 + t) * RS + r];
         if (r < rows) P.Y[(size_t)t * P.N + n0 + r] = v;
     }
+}
+
+// ---------------------------------------------------------------- all in flight
+//
+// When K / 64 is a multiple of NJ = 8 (and at most 16 * NJ), each warp owns NJ
+// consecutive groups of its tile and copies all of them at once: the ring
+// never refills, the group loop is fully unrolled with immediate offsets, and
+// the codec is resolved once per CTA, which leaves per group little beyond the
+// decode, the four MMAs and the rescale.  A CTA has K / (64 NJ) warps.
+
+constexpr int NJ = 8;
+
+template <int NT>
+struct FullSmem {
+    static constexpr int RED_STRIDE = 17;
+    __host__ __device__ static constexpr int rings(int kw) { return kw * NJ * STAGE; }
+    __host__ __device__ static constexpr int bytes(int kw) { return rings(kw) + kw * NT * 8 * RED_STRIDE * 4; }
+};
+
+// Group R of the warp: wait for its copy, decode, MMA against the activation
+// fragments, rescale into acc.
+// Activation fragment of group R for token row pointer xr: the lane's 16 k.
+// (volatile, so that the compiler keeps the loads where they are written: the
+// up-front loads must not sink to their uses)
+template <int R>
+__device__ __forceinline__ void load_x(const __nv_bfloat16 *xr, uint32_t (&xb)[8]) {
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xb[0]), "=r"(xb[1]), "=r"(xb[2]), "=r"(xb[3]) : "l"(xr + R * GROUP));
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xb[4]), "=r"(xb[5]), "=r"(xb[6]), "=r"(xb[7]) : "l"(xr + R * GROUP + 8));
+}
+
+// xpre: the activation fragments of every group, loaded up front (NT == 1);
+// otherwise each group loads its own from xr[nt].
+template <int NT, int CODEC, int R>
+__device__ __forceinline__ void full_group(const uint8_t *ring, int lane, int g,
+                                           const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[NJ][8],
+                                           float (&acc)[NT][4]) {
+    uint32_t xb[NT][8];
+    if (NT == 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xb[0][e] = xpre[R][e];
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) load_x<R>(xr[nt], xb[nt]);
+    }
+    cp_async_wait<NJ - 1 - R>();                      // groups 0..R of this lane have landed
+    __syncwarp();                                     // ... and of every lane
+    const uint8_t *st = ring + R * STAGE;
+    const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * 16);
+    const uint32_t hw = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
+    const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + 640 + g * 4);
+    uint32_t a[4][4];
+    decode_tile(CODEC, cw, hw, a);
+    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t bf[2] = {xb[nt][2 * q], xb[nt][2 * q + 1]};
+            mma_bf16_16816(p, a[q], bf, p);
+        }
+        acc[nt][0] = fmaf(sc.x, p[0], acc[nt][0]);
+        acc[nt][1] = fmaf(sc.x, p[1], acc[nt][1]);
+        acc[nt][2] = fmaf(sc.y, p[2], acc[nt][2]);
+        acc[nt][3] = fmaf(sc.y, p[3], acc[nt][3]);
+    }
+}
+
+template <int NT, int CODEC, int... R>
+__device__ __forceinline__ void full_groups(std::integer_sequence<int, R...>, const uint8_t *ring, int lane, int g,
+                                            const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[NJ][8],
+                                            float (&acc)[NT][4]) {
+    (full_group<NT, CODEC, R>(ring, lane, g, xr, xpre, acc), ...);
+}
+
+template <int... R>
+__device__ __forceinline__ void load_x_all(std::integer_sequence<int, R...>, const __nv_bfloat16 *xr,
+                                           uint32_t (&xpre)[NJ][8]) {
+    (load_x<R>(xr, xpre[R]), ...);
+}
+
+template <int NT, int CODEC>
+__device__ __forceinline__ void full_tile(const SkinnyArgs &args, const SkinnyParent &P, int tile, uint8_t *smem) {
+    constexpr int RS = FullSmem<NT>::RED_STRIDE;
+    constexpr int T8 = 8 * NT;
+    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    const int KW = blockDim.x >> 5;
+    const int b = tile / TILES, w = tile % TILES;
+    const int G = args.G;
+    const int kw = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int T = args.T;
+    const int gb = kw * NJ;                           // this warp's first group
+    uint8_t *ring = smem + kw * NJ * STAGE;
+    float *red = reinterpret_cast<float *>(smem + FullSmem<NT>::rings(KW));
+
+    // per-lane copy plan (as the ring kernel's): every lane its 16-byte code
+    // chunk; lanes 8..15 the int5 high words; lanes 16..17 the scale pairs
+    const uint8_t *src = P.packed + ((size_t)b * G + gb) * UB + w * 512 + lane * 16;
+    const bool cp_hi = CODEC == 5 && lane >= 8 && lane < 16;
+    const bool cp_sc = lane >= 16 && lane < 18;
+    const int ex_dst = cp_hi ? 512 + (lane - 8) * 16 : 640 + (lane - 16) * 16;
+    const int ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
+                             : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - (w * 512 + lane * 16);
+#pragma unroll
+    for (int r = 0; r < NJ; ++r) {
+        cp_async16(ring + r * STAGE + lane * 16, src + r * UB);
+        if (cp_hi || cp_sc) cp_async16(ring + r * STAGE + ex_dst, src + r * UB + ex_src);
+        cp_async_commit();
+    }
+    // Programmatic dependent launch: with one token tile the next kernel in the
+    // stream may start as soon as this CTA's weight copies are issued (its own
+    // weight stream then overlaps this kernel's tail); with more token tiles
+    // the CTA's compute is longer and an early start measured slower, so the
+    // trigger waits until this CTA's groups are done.
+    if (NT == 1 && threadIdx.x == 0) pdl_launch_dependents();
+    pdl_wait_prior();   // X and Y may belong to the previous kernel
+
+    // activation fragments: token 8*nt + g, k = 64*(gb + r) + 16c.  Lanes of
+    // tokens >= T read row T - 1 instead: their MMA columns are never written,
+    // and every lane then runs the same loads with no branch.  With one token
+    // tile the fragments of all NJ groups are loaded up front, in the shadow
+    // of the weight copies; otherwise lanes with c == 0 pull the rows' lines
+    // into L1 and each group loads its own.
+    const __nv_bfloat16 *xr[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        xr[nt] = args.X + (size_t)min(nt * 8 + g, T - 1) * args.K + (size_t)gb * GROUP + 16 * c;
+    uint32_t xpre[NJ][8];
+    if (NT == 1) {
+        load_x_all(std::make_integer_sequence<int, NJ>{}, xr[0], xpre);
+    } else if (c == 0) {
+#pragma unroll
+        for (int r = 0; r < NJ; ++r)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) prefetch_l1(xr[nt] + r * GROUP);
+    }
+
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    full_groups<NT, CODEC>(std::make_integer_sequence<int, NJ>{}, ring, lane, g, xr, xpre, acc);
+    if (NT > 1 && threadIdx.x == 0) pdl_launch_dependents();
+
+    // ---- combine the warps' partials in warp order and write Y
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int t = nt * 8 + 2 * c;
+        float *rw = red + (kw * T8) * RS;
+        rw[t * RS + g] = acc[nt][0];
+        rw[(t + 1) * RS + g] = acc[nt][1];
+        rw[t * RS + g + 8] = acc[nt][2];
+        rw[(t + 1) * RS + g + 8] = acc[nt][3];
+    }
+    __syncthreads();
+    const int n0 = tile * 16;
+    const int rows = min(16, P.N - n0);
+    for (int e = threadIdx.x; e < T * 16; e += KW * 32) {
+        const int t = e >> 4, r = e & 15;
+        float v = red[t * RS + r];
+        for (int q = 1; q < KW; ++q) v += red[(q * T8 + t) * RS + r];
+        if (r < rows) P.Y[(size_t)t * P.N + n0 + r] = v;
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(16 * 32) skinny_full_kernel(const __grid_constant__ SkinnyArgs args) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    int pi = 0;
+#pragma unroll
+    for (int i = 1; i < MAX_PARENTS; ++i)
+        if (i < args.nparents && (int)blockIdx.x >= args.p[i].cta_begin) pi = i;
+    const SkinnyParent &P = args.p[pi];
+    const int tile = blockIdx.x - P.cta_begin;
+    if (P.codec == 4) full_tile<NT, 4>(args, P, tile, smem);
+    else full_tile<NT, 5>(args, P, tile, smem);
+}
+
+template <int NT>
+static cudaError_t launch_full_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int kw = a.G / NJ;
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(skinny_full_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FullSmem<NT>::bytes(16));
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kw * 32, 1, 1);
+    cfg.dynamicSmemBytes = FullSmem<NT>::bytes(kw);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, skinny_full_kernel<NT>, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Whether the all-in-flight kernel serves K / 64 = G groups.
+bool skinny_full_supported(int G) { return G % NJ == 0 && G / NJ >= 1 && G / NJ <= 16; }
+
+cudaError_t launch_skinny_full(const SkinnyArgs &a, int nt, int grid, bool pdl, cudaStream_t stream) {
+    if (!skinny_full_supported(a.G)) return cudaErrorInvalidValue;
+    switch (nt) {
+        case 1: return launch_full_t<1>(a, grid, pdl, stream);
+        case 2: return launch_full_t<2>(a, grid, pdl, stream);
+        case 4: return launch_full_t<4>(a, grid, pdl, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <int NT, int KW>

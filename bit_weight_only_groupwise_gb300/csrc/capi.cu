@@ -14,8 +14,8 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
                         cudaStream_t stream);
 cudaError_t launch_fence(cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
-bool skinny_full_supported(int G);
-cudaError_t launch_skinny_full(const SkinnyArgs &a, int nt, int grid, bool pdl, cudaStream_t stream);
+int skinny_line_groups(int G, int nj_pref);
+cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream);
 cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
                         cudaStream_t stream, int *launches);
 }  // namespace qg
@@ -227,8 +227,8 @@ static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, float *Y, int c
 
 // Tuning knob read once from the environment, for sweeps only:
 // QGEMM_SKINNY_WARPS sets the warps (K slices) per CTA of the small-T ring
-// kernel; QGEMM_SKINNY_FULL=0 keeps the ring kernel where the all-in-flight
-// kernel would serve.
+// kernel; QGEMM_SKINNY_LINE selects the groups per warp of the straight-line
+// kernel (16 or 8; 0 keeps the ring kernel).
 static int env_int(const char *name, int dflt) {
     const char *v = getenv(name);
     return (v && *v) ? atoi(v) : dflt;
@@ -238,7 +238,7 @@ static int env_int(const char *name, int dflt) {
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
                                 float *const *Ys, cudaStream_t stream) {
     static const int kw = env_int("QGEMM_SKINNY_WARPS", 8);
-    static const bool full = env_int("QGEMM_SKINNY_FULL", 1) != 0;
+    static const int line = env_int("QGEMM_SKINNY_LINE", 8);
     const int route = choose_route(T);
     const int K = plans[0]->K;
     const int G = K / GROUP;
@@ -273,9 +273,9 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     a.T = T;
     a.K = K;
     a.G = G;
-    const cudaError_t e = (full && skinny_full_supported(G))
-                              ? launch_skinny_full(a, route_tokens(route) / 8, grid, pdl, stream)
-                              : launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, stream);
+    const int nj = skinny_line_groups(G, line);
+    const cudaError_t e = nj ? launch_skinny_line(a, route_tokens(route) / 8, nj, grid, pdl, stream)
+                             : launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, stream);
     if (e != cudaSuccess) return QGEMM_ERR_CUDA;
     g_launches.fetch_add(1);
     return QGEMM_OK;

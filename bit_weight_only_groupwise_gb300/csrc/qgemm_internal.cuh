@@ -230,17 +230,25 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     return d;
 }
 
+// (a & b) | c as one three-input logic instruction (truth table 0xEA); the
+// compiler otherwise splits the mask and the OR of two constants into two.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Codes (i, i+4) of a nibble word as an exact bf16x2 pair of integers.
 template <int SHIFT>
 __device__ __forceinline__ uint32_t dec4_pair(uint32_t w) {
-    return bf16x2_sub(((w >> SHIFT) & 0x000F000Fu) | 0x43004300u, 0x43084308u);   // - (128 + 8)
+    return bf16x2_sub(and_or(w >> SHIFT, 0x000F000Fu, 0x43004300u), 0x43084308u);   // - (128 + 8)
 }
 
 // int5: nibble pair plus the two high bits taken from the lane's high word.
 template <int SHIFT, int HSH>
 __device__ __forceinline__ uint32_t dec5_pair(uint32_t w, uint32_t h) {
-    uint32_t hb = (HSH >= 0 ? (h >> HSH) : (h << (-HSH))) & 0x00100010u;
-    return bf16x2_sub(((w >> SHIFT) & 0x000F000Fu) | hb | 0x43004300u, 0x43104310u);   // - (128 + 16)
+    const uint32_t hm = and_or(HSH >= 0 ? (h >> HSH) : (h << (-HSH)), 0x00100010u, 0x43004300u);
+    return bf16x2_sub(and_or(w >> SHIFT, 0x000F000Fu, hm), 0x43104310u);   // - (128 + 16)
 }
 
 }  // namespace qg

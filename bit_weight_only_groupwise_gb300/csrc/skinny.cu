@@ -237,25 +237,25 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
     }
 }
 
-// ---------------------------------------------------------------- all in flight
+// ---------------------------------------------------------------- straight-line kernels
 //
-// When K / 64 is a multiple of NJ = 8 (and at most 16 * NJ), each warp owns NJ
-// consecutive groups of its tile and copies all of them at once: the ring
-// never refills, the group loop is fully unrolled with immediate offsets, and
-// the codec is resolved once per CTA, which leaves per group little beyond the
-// decode, the four MMAs and the rescale.  A CTA has K / (64 NJ) warps.
+// When K / 64 is a multiple of NJ, each warp owns NJ consecutive groups of its
+// tile.  Its copies go through a private ring of RG stages (RG == NJ: all of
+// them in flight at once; RG < NJ: the stage a group was read from is refilled
+// with group + RG right after the read), the group loop is fully unrolled
+// with immediate offsets, and the codec is resolved once per CTA, which leaves
+// per group little beyond the decode, the four MMAs and the rescale.  A CTA
+// has K / (64 NJ) warps.  A smaller ring lets more CTAs share an SM, so that
+// the next call's CTAs can start their weight stream while this call's CTAs
+// still compute.
 
-constexpr int NJ = 8;
-
-template <int NT>
-struct FullSmem {
+template <int NJ, int RG, int NT>
+struct LineSmem {
     static constexpr int RED_STRIDE = 17;
-    __host__ __device__ static constexpr int rings(int kw) { return kw * NJ * STAGE; }
+    __host__ __device__ static constexpr int rings(int kw) { return kw * RG * STAGE; }
     __host__ __device__ static constexpr int bytes(int kw) { return rings(kw) + kw * NT * 8 * RED_STRIDE * 4; }
 };
 
-// Group R of the warp: wait for its copy, decode, MMA against the activation
-// fragments, rescale into acc.
 // Activation fragment of group R for token row pointer xr: the lane's 16 k.
 // (volatile, so that the compiler keeps the loads where they are written: the
 // up-front loads must not sink to their uses)
@@ -267,26 +267,55 @@ __device__ __forceinline__ void load_x(const __nv_bfloat16 *xr, uint32_t (&xb)[8
                  : "=r"(xb[4]), "=r"(xb[5]), "=r"(xb[6]), "=r"(xb[7]) : "l"(xr + R * GROUP + 8));
 }
 
-// xpre: the activation fragments of every group, loaded up front (NT == 1);
-// otherwise each group loads its own from xr[nt].
-template <int NT, int CODEC, int R>
-__device__ __forceinline__ void full_group(const uint8_t *ring, int lane, int g,
-                                           const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[NJ][8],
+// The copies of one lane for the warp's groups: its 16-byte code chunk, and
+// for lanes 8..15 (int5 high words) and 16..17 (scale pairs) one more chunk.
+struct LaneCopies {
+    const uint8_t *src;      // the lane's code chunk of the warp's first group
+    int ex_dst, ex_src;      // the extra chunk: offset in the stage, offset from src
+    bool ex;
+};
+
+template <int UB, int RG, int R>
+__device__ __forceinline__ void issue_group(uint8_t *ring, const LaneCopies &lc, int lane) {
+    uint8_t *st = ring + (R % RG) * STAGE;
+    cp_async16(st + lane * 16, lc.src + R * UB);
+    if (lc.ex) cp_async16(st + lc.ex_dst, lc.src + R * UB + lc.ex_src);
+    cp_async_commit();
+}
+
+template <int UB, int RG, int... R>
+__device__ __forceinline__ void issue_groups(std::integer_sequence<int, R...>, uint8_t *ring, const LaneCopies &lc,
+                                             int lane) {
+    (issue_group<UB, RG, R>(ring, lc, lane), ...);
+}
+
+// Group R of the warp: wait for its copy, refill its stage, decode, MMA
+// against the activation fragments, rescale into acc.  xpre holds the
+// activation fragments of every group when they were loaded up front.
+template <int NT, int CODEC, int NJ, int RG, int XP, int R>
+__device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, int lane, int g,
+                                           const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[XP][8],
                                            float (&acc)[NT][4]) {
+    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    constexpr int ISSUED = RG + R < NJ ? RG + R : NJ;     // groups whose copies are issued
     uint32_t xb[NT][8];
-    if (NT == 1) {
+    if (XP == NJ) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) xb[0][e] = xpre[R][e];
     } else {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) load_x<R>(xr[nt], xb[nt]);
     }
-    cp_async_wait<NJ - 1 - R>();                      // groups 0..R of this lane have landed
-    __syncwarp();                                     // ... and of every lane
-    const uint8_t *st = ring + R * STAGE;
+    cp_async_wait<ISSUED - 1 - R>();                   // groups 0..R of this lane have landed
+    __syncwarp();                                      // ... and of every lane
+    const uint8_t *st = ring + (R % RG) * STAGE;
     const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * 16);
     const uint32_t hw = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
     const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + 640 + g * 4);
+    if (R + RG < NJ) {
+        __syncwarp();                                  // every lane has read the stage
+        issue_group<UB, RG, R + RG>(ring, lc, lane);
+    }
     uint32_t a[4][4];
     decode_tile(CODEC, cw, hw, a);
     const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
@@ -305,24 +334,25 @@ __device__ __forceinline__ void full_group(const uint8_t *ring, int lane, int g,
     }
 }
 
-template <int NT, int CODEC, int... R>
-__device__ __forceinline__ void full_groups(std::integer_sequence<int, R...>, const uint8_t *ring, int lane, int g,
-                                            const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[NJ][8],
-                                            float (&acc)[NT][4]) {
-    (full_group<NT, CODEC, R>(ring, lane, g, xr, xpre, acc), ...);
+template <int NT, int CODEC, int NJ, int RG, int XP, int... R>
+__device__ __forceinline__ void line_groups(std::integer_sequence<int, R...>, uint8_t *ring, const LaneCopies &lc,
+                                            int lane, int g, const __nv_bfloat16 *const (&xr)[NT],
+                                            const uint32_t (&xpre)[XP][8], float (&acc)[NT][4]) {
+    (line_group<NT, CODEC, NJ, RG, XP, R>(ring, lc, lane, g, xr, xpre, acc), ...);
 }
 
-template <int... R>
+template <int XP, int... R>
 __device__ __forceinline__ void load_x_all(std::integer_sequence<int, R...>, const __nv_bfloat16 *xr,
-                                           uint32_t (&xpre)[NJ][8]) {
+                                           uint32_t (&xpre)[XP][8]) {
     (load_x<R>(xr, xpre[R]), ...);
 }
 
-template <int NT, int CODEC>
-__device__ __forceinline__ void full_tile(const SkinnyArgs &args, const SkinnyParent &P, int tile, uint8_t *smem) {
-    constexpr int RS = FullSmem<NT>::RED_STRIDE;
+template <int NT, int CODEC, int NJ, int RG>
+__device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyParent &P, int tile, uint8_t *smem) {
+    constexpr int RS = LineSmem<NJ, RG, NT>::RED_STRIDE;
     constexpr int T8 = 8 * NT;
     constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    constexpr int XP = (NT == 1 && NJ <= 8) ? NJ : 1;   // activation fragments loaded up front
     const int KW = blockDim.x >> 5;
     const int b = tile / TILES, w = tile % TILES;
     const int G = args.G;
@@ -330,44 +360,41 @@ __device__ __forceinline__ void full_tile(const SkinnyArgs &args, const SkinnyPa
     const int g = lane >> 2, c = lane & 3;
     const int T = args.T;
     const int gb = kw * NJ;                           // this warp's first group
-    uint8_t *ring = smem + kw * NJ * STAGE;
-    float *red = reinterpret_cast<float *>(smem + FullSmem<NT>::rings(KW));
+    uint8_t *ring = smem + kw * RG * STAGE;
+    float *red = reinterpret_cast<float *>(smem + LineSmem<NJ, RG, NT>::rings(KW));
 
     // per-lane copy plan (as the ring kernel's): every lane its 16-byte code
     // chunk; lanes 8..15 the int5 high words; lanes 16..17 the scale pairs
-    const uint8_t *src = P.packed + ((size_t)b * G + gb) * UB + w * 512 + lane * 16;
     const bool cp_hi = CODEC == 5 && lane >= 8 && lane < 16;
-    const bool cp_sc = lane >= 16 && lane < 18;
-    const int ex_dst = cp_hi ? 512 + (lane - 8) * 16 : 640 + (lane - 16) * 16;
-    const int ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
-                             : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - (w * 512 + lane * 16);
-#pragma unroll
-    for (int r = 0; r < NJ; ++r) {
-        cp_async16(ring + r * STAGE + lane * 16, src + r * UB);
-        if (cp_hi || cp_sc) cp_async16(ring + r * STAGE + ex_dst, src + r * UB + ex_src);
-        cp_async_commit();
-    }
+    LaneCopies lc;
+    lc.src = P.packed + ((size_t)b * G + gb) * UB + w * 512 + lane * 16;
+    lc.ex = cp_hi || (lane >= 16 && lane < 18);
+    lc.ex_dst = cp_hi ? 512 + (lane - 8) * 16 : 640 + (lane - 16) * 16;
+    lc.ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
+                      : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - (w * 512 + lane * 16);
+    issue_groups<UB, RG>(std::make_integer_sequence<int, RG>{}, ring, lc, lane);
     // Programmatic dependent launch: with one token tile the next kernel in the
-    // stream may start as soon as this CTA's weight copies are issued (its own
-    // weight stream then overlaps this kernel's tail); with more token tiles
-    // the CTA's compute is longer and an early start measured slower, so the
-    // trigger waits until this CTA's groups are done.
-    if (NT == 1 && threadIdx.x == 0) pdl_launch_dependents();
+    // stream may start once this CTA's weight copies are issued and the
+    // previous kernel has finished (its own weight stream then overlaps this
+    // kernel's compute, and no kernel runs more than one call ahead); with
+    // more token tiles the CTA's compute is longer and an early start measured
+    // slower, so the trigger waits until this CTA's groups are done.
     pdl_wait_prior();   // X and Y may belong to the previous kernel
+    if (NT == 1 && threadIdx.x == 0) pdl_launch_dependents();
 
     // activation fragments: token 8*nt + g, k = 64*(gb + r) + 16c.  Lanes of
     // tokens >= T read row T - 1 instead: their MMA columns are never written,
     // and every lane then runs the same loads with no branch.  With one token
-    // tile the fragments of all NJ groups are loaded up front, in the shadow
-    // of the weight copies; otherwise lanes with c == 0 pull the rows' lines
-    // into L1 and each group loads its own.
+    // tile and few groups per warp the fragments of all groups are loaded up
+    // front, in the shadow of the weight copies; otherwise lanes with c == 0
+    // pull the rows' lines into L1 and each group loads its own.
     const __nv_bfloat16 *xr[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
         xr[nt] = args.X + (size_t)min(nt * 8 + g, T - 1) * args.K + (size_t)gb * GROUP + 16 * c;
-    uint32_t xpre[NJ][8];
-    if (NT == 1) {
-        load_x_all(std::make_integer_sequence<int, NJ>{}, xr[0], xpre);
+    uint32_t xpre[XP][8];
+    if (XP == NJ) {
+        load_x_all<XP>(std::make_integer_sequence<int, XP>{}, xr[0], xpre);
     } else if (c == 0) {
 #pragma unroll
         for (int r = 0; r < NJ; ++r)
@@ -380,7 +407,7 @@ __device__ __forceinline__ void full_tile(const SkinnyArgs &args, const SkinnyPa
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    full_groups<NT, CODEC>(std::make_integer_sequence<int, NJ>{}, ring, lane, g, xr, xpre, acc);
+    line_groups<NT, CODEC, NJ, RG, XP>(std::make_integer_sequence<int, NJ>{}, ring, lc, lane, g, xr, xpre, acc);
     if (NT > 1 && threadIdx.x == 0) pdl_launch_dependents();
 
     // ---- combine the warps' partials in warp order and write Y
@@ -404,8 +431,8 @@ __device__ __forceinline__ void full_tile(const SkinnyArgs &args, const SkinnyPa
     }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(16 * 32) skinny_full_kernel(const __grid_constant__ SkinnyArgs args) {
+template <int NT, int NJ, int RG>
+__global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_constant__ SkinnyArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
     int pi = 0;
 #pragma unroll
@@ -413,12 +440,12 @@ __global__ void __launch_bounds__(16 * 32) skinny_full_kernel(const __grid_const
         if (i < args.nparents && (int)blockIdx.x >= args.p[i].cta_begin) pi = i;
     const SkinnyParent &P = args.p[pi];
     const int tile = blockIdx.x - P.cta_begin;
-    if (P.codec == 4) full_tile<NT, 4>(args, P, tile, smem);
-    else full_tile<NT, 5>(args, P, tile, smem);
+    if (P.codec == 4) line_tile<NT, 4, NJ, RG>(args, P, tile, smem);
+    else line_tile<NT, 5, NJ, RG>(args, P, tile, smem);
 }
 
-template <int NT>
-static cudaError_t launch_full_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
+template <int NT, int NJ, int RG>
+static cudaError_t launch_line_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
     static bool done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -426,34 +453,48 @@ static cudaError_t launch_full_t(const SkinnyArgs &a, int grid, bool pdl, cudaSt
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int kw = a.G / NJ;
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(skinny_full_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 FullSmem<NT>::bytes(16));
+        e = cudaFuncSetAttribute(skinny_line_kernel<NT, NJ, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 LineSmem<NJ, RG, NT>::bytes(16));
         if (e != cudaSuccess) return e;
         done[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kw * 32, 1, 1);
-    cfg.dynamicSmemBytes = FullSmem<NT>::bytes(kw);
+    cfg.dynamicSmemBytes = LineSmem<NJ, RG, NT>::bytes(kw);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, skinny_full_kernel<NT>, a);
+    e = cudaLaunchKernelEx(&cfg, skinny_line_kernel<NT, NJ, RG>, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Whether the all-in-flight kernel serves K / 64 = G groups.
-bool skinny_full_supported(int G) { return G % NJ == 0 && G / NJ >= 1 && G / NJ <= 16; }
+// Groups per warp of the straight-line kernel that serves K / 64 = G groups
+// (at most 16 warps per CTA): 0 if none does.  nj_pref 16 selects 16 groups
+// per warp through an 8-stage ring where G allows, 8 selects 8 groups per
+// warp all in flight.
+int skinny_line_groups(int G, int nj_pref) {
+    if (nj_pref == 16 && G % 16 == 0 && G / 16 <= 16) return 16;
+    if (nj_pref >= 8 && G % 8 == 0 && G / 8 <= 16) return 8;
+    return 0;
+}
 
-cudaError_t launch_skinny_full(const SkinnyArgs &a, int nt, int grid, bool pdl, cudaStream_t stream) {
-    if (!skinny_full_supported(a.G)) return cudaErrorInvalidValue;
-    switch (nt) {
-        case 1: return launch_full_t<1>(a, grid, pdl, stream);
-        case 2: return launch_full_t<2>(a, grid, pdl, stream);
-        case 4: return launch_full_t<4>(a, grid, pdl, stream);
+cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream) {
+    if (nj == 16 && a.G % 16 == 0 && a.G / 16 <= 16) {
+        switch (nt) {
+            case 1: return launch_line_t<1, 16, 8>(a, grid, pdl, stream);
+            case 2: return launch_line_t<2, 16, 8>(a, grid, pdl, stream);
+            case 4: return launch_line_t<4, 16, 8>(a, grid, pdl, stream);
+        }
+    } else if (nj == 8 && a.G % 8 == 0 && a.G / 8 <= 16) {
+        switch (nt) {
+            case 1: return launch_line_t<1, 8, 8>(a, grid, pdl, stream);
+            case 2: return launch_line_t<2, 8, 8>(a, grid, pdl, stream);
+            case 4: return launch_line_t<4, 8, 8>(a, grid, pdl, stream);
+        }
     }
     return cudaErrorInvalidValue;
 }

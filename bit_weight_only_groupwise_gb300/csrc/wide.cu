@@ -25,8 +25,8 @@
 //   warps 8..15   epilogue: read P_g from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
 //                 (packed f32x2 FMA), then write Y.
-// Tensor memory: NP = 2 P buffers of 128 columns (the MMA fills one while the
-// epilogue drains the other) and NS A stages of 32 columns (64 bf16 per row).
+// Tensor memory: NP P buffers of 128 columns (the MMA fills one while the
+// epilogue drains another) and NA A stages of 32 columns (64 bf16 per row).
 // Synchronisation per group g (stage s = g mod NS):
 //   go[s]     completes when A_g is in tensor memory (4 dequant arrivals),
 //             X_g has landed (TMA transaction bytes + 1 arrival) and the P
@@ -49,7 +49,8 @@ namespace wide {
 
 constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
 constexpr int BN = 128;                   // tokens per CTA (MMA N)
-constexpr int NS = 8;                     // activation / A stages (one ring index)
+constexpr int NS = 8;                     // activation stages (and the go / done ring)
+constexpr int NA = 8;                     // A stages in tensor memory (group g uses g % NA)
 constexpr int NWP = 8;                    // weight stages, each a pair of consecutive groups' units
 constexpr int NP = 2;                     // P buffers in tensor memory
 constexpr int DQ_WARPS = 4;               // one dequant warp per TMEM lane quarter
@@ -59,12 +60,13 @@ constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
 constexpr int GO_COUNT = DQ_WARPS + 1 + EPI_WARPS;
 constexpr int SC_RING = 16;               // groups of scales in flight
 // the dequant stores the scale of group g once the epilogue has finished group g - NS - NP - 1
-static_assert(SC_RING >= NS + NP + 2, "scale ring shorter than the dequant lead");
+static_assert(SC_RING >= NA + NP + 2, "scale ring shorter than the dequant lead");
+static_assert(NA <= NS && NA % 2 == 0, "A stages: even (pairs of groups) and no more than the ring");
 static_assert(NS > NP, "go barrier phases need more stages than P buffers");
 constexpr int X_STAGE = BN * GROUP * 2;   // 16 KB
 constexpr int P_COL = 0;                  // P buffers: columns [0, 128*NP)
-constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NS)
-static_assert(A_COL + 32 * NS <= 512, "tensor memory budget");
+constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NA)
+static_assert(A_COL + 32 * NA <= 512, "tensor memory budget");
 constexpr int TMEM_COLS = 512;
 
 struct Smem {
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             if (!(ok = mbar_wait_warp(&go[s], (g / NS) & 1, args.status))) break;
             tc_fence_after();
             const uint32_t d = tmem + P_COL + pb * BN;
-            const uint32_t a = tmem + A_COL + s * 32;
+            const uint32_t a = tmem + A_COL + (g % NA) * 32;
             const uint32_t b0 = smem_u32(xs + s * X_STAGE);
             // one elected lane per instruction: measured cheaper to issue than
             // one elected block of four
@@ -342,18 +344,20 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 }
             }
             // the A stages of both groups are free once the MMAs of groups
-            // g0 - NS and g0 + 1 - NS have completed
-            if (two && g0 + 1 >= NS) {
-                // (g0 >= NS too: NS is even)
-                ok = __all_sync(0xffffffffu, mbar_wait2(&done[g0 % NS], ((g0 / NS) - 1) & 1, &done[(g0 + 1) % NS],
-                                                        (((g0 + 1) / NS) - 1) & 1, args.status));
-            } else if (g0 >= NS) {
-                ok = mbar_wait_warp(&done[g0 % NS], ((g0 / NS) - 1) & 1, args.status);
+            // g0 - NA and g0 + 1 - NA have completed
+            if (two && g0 + 1 >= NA) {
+                // (g0 >= NA too: both are even)
+                const int h0 = g0 - NA, h1 = g0 + 1 - NA;
+                ok = __all_sync(0xffffffffu, mbar_wait2(&done[h0 % NS], (h0 / NS) & 1, &done[h1 % NS], (h1 / NS) & 1,
+                                                        args.status));
+            } else if (g0 >= NA) {
+                const int h0 = g0 - NA;
+                ok = mbar_wait_warp(&done[h0 % NS], (h0 / NS) & 1, args.status);
             }
             if (!ok) break;
             tc_fence_after();
-            tc_st32(tmem + tlane + A_COL + (g0 % NS) * 32, av[0]);
-            if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NS) * 32, av[1]);
+            tc_st32(tmem + tlane + A_COL + (g0 % NA) * 32, av[0]);
+            if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NA) * 32, av[1]);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();

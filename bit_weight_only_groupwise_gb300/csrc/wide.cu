@@ -380,7 +380,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         bool ok = true;
         for (int g = 0; g < G; ++g) {
             const int ps = g % NP;
-            if (!(ok = mbar_wait_warp(&done[g % NS], (g / NS) & 1, args.status))) break;
+            // polled: the epilogue gates the MMAs of group g + NP
+            if (!(ok = mbar_spin_warp(&done[g % NS], (g / NS) & 1, args.status))) break;
             tc_fence_after();
             const float s = sc_ring[(g % SC_RING) * BM + r];
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;

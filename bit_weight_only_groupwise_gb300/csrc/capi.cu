@@ -45,7 +45,18 @@ static int route_tokens(int route) {
 
 // Narrowest tile that covers T (the padded width sets the cost, not the live
 // column count).
+static int env_route() {
+    // QGEMM_ROUTE forces a route wherever its token tile covers T (for route
+    // sweeps only; unset in normal use)
+    const char *v = getenv("QGEMM_ROUTE");
+    return (v && *v) ? atoi(v) : -1;
+}
+
 static int choose_route(int T) {
+    static const int forced = env_route();
+    if (forced == ROUTE_WIDE128) return ROUTE_WIDE128;
+    if (forced == ROUTE_SKINNY32 && T <= 32) return ROUTE_SKINNY32;
+    if (forced == ROUTE_SKINNY16 && T <= 16) return ROUTE_SKINNY16;
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
     if (T <= 32) return ROUTE_SKINNY32;

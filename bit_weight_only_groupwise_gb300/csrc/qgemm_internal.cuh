@@ -82,12 +82,12 @@ struct SkinnyArgs {
     unsigned int *status;    // device status word
 };
 
-// The wide route's grid has ceil(N/128) x ceil(T/128) CTAs per parent.
+// The wide route covers ceil(N/128) x ceil(T/128) output tiles per parent.
 struct WideParent {
     const uint8_t *packed;   // units of this parent
     float *Y;                // [T][N]
     int N, codec;
-    int cta_begin;           // first CTA of this parent in its launch
+    int cta_begin;           // first output tile of this parent in its launch
     int nblocks;             // 128-row blocks
 };
 

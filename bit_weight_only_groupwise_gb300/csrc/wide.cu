@@ -87,8 +87,24 @@ struct WideArgs {
     int nparents;
     int T, K, G;
     int ntt;              // token tiles
+    int ntiles;           // output tiles of all parents (parent i owns p[i].cta_begin ...)
     unsigned int *status;
 };
+
+// An output tile: its parent, 128-row block and 128-token tile.
+struct WideTile {
+    const WideParent *P;
+    int blk, tt;
+};
+
+__device__ __forceinline__ WideTile wide_tile(const WideArgs &a, int tile) {
+    int pi = 0;
+#pragma unroll
+    for (int i = 1; i < MAX_PARENTS; ++i)
+        if (i < a.nparents && tile >= a.p[i].cta_begin) pi = i;
+    const int local = tile - a.p[pi].cta_begin;
+    return {&a.p[pi], local / a.ntt, local % a.ntt};
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -202,18 +218,17 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
     volatile uint32_t *abort_flag = taddr_slot + 1;
 
-    // ---- which parent, row block and token tile
-    int pi = 0;
-#pragma unroll
-    for (int i = 1; i < MAX_PARENTS; ++i)
-        if (i < args.nparents && (int)blockIdx.x >= args.p[i].cta_begin) pi = i;
-    const WideParent &P = args.p[pi];
-    const int local = blockIdx.x - P.cta_begin;
-    const int blk = local / args.ntt, tt = local % args.ntt;
+    // ---- this CTA's work: output tiles blockIdx.x, blockIdx.x + gridDim.x,
+    // ... of all parents (parent i owns tiles [p[i].cta_begin, p[i].cta_begin
+    // + nblocks * ntt)); every role walks the same steps gi = it * G + k over
+    // the groups k of its it-th tile, so the rings and barrier phases run on
+    // across tiles and the next tile's copies and MMAs overlap this tile's
+    // epilogue
     const int G = args.G, T = args.T;
+    const int my_tiles = (int)blockIdx.x < args.ntiles ? (args.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int steps = my_tiles * G;
     constexpr int codec = CODEC;
     constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
-    const uint8_t *units = P.packed + (size_t)blk * G * UB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -234,47 +249,56 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const uint32_t tmem = *taddr_slot;
 
     if (warp == 0) {
-        // ---------------- weight producer: the units of groups (2j, 2j+1) in one
-        // 1-D bulk copy (a row block's units are consecutive in memory)
+        // ---------------- weight producer: the units of groups (2j, 2j+1) of a
+        // tile in one 1-D bulk copy (a row block's units are consecutive)
         bool ok = true;
-        for (int j = 0; j < (G + 1) / 2; ++j) {
-            const int wsl = j % NWP;
-            const uint32_t bytes = (2 * j + 1 < G ? 2 : 1) * UB;
-            if (j >= NWP && !(ok = mbar_wait_warp(&w_empty[wsl], ((j / NWP) - 1) & 1, args.status))) break;
-            if (elect_one()) {
-                mbar_arrive_expect_tx(&w_full[wsl], bytes);
-                bulk_g2s(ws + wsl * 2 * UNIT5, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
+        int jp = 0;                                   // weight stages used so far
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
+            const uint8_t *units = tr.P->packed + (size_t)tr.blk * G * UB;
+            for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
+                const int wsl = jp % NWP;
+                const uint32_t bytes = (2 * j + 1 < G ? 2 : 1) * UB;
+                if (jp >= NWP && !(ok = mbar_wait_warp(&w_empty[wsl], ((jp / NWP) - 1) & 1, args.status))) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&w_full[wsl], bytes);
+                    bulk_g2s(ws + wsl * 2 * UNIT5, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp == 2) {
         // ---------------- activation producer: 128B-swizzled X tiles, 2-D TMA
         bool ok = true;
-        for (int g = 0; g < G; ++g) {
-            const int s = g % NS;
-            if (g >= NS && !(ok = mbar_wait_warp(&done[s], ((g / NS) - 1) & 1, args.status))) break;
-            if (elect_one()) {
-                mbar_arrive_expect_tx(&go[s], X_STAGE);
-                tma_load_2d(xs + s * X_STAGE, &xmap, g * GROUP, tt * BN, &go[s]);
+        int gi = 0;
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
+            for (int k = 0; k < G; ++k, ++gi) {
+                const int s = gi % NS;
+                if (gi >= NS && !(ok = mbar_wait_warp(&done[s], ((gi / NS) - 1) & 1, args.status))) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&go[s], X_STAGE);
+                    tma_load_2d(xs + s * X_STAGE, &xmap, k * GROUP, tr.tt * BN, &go[s]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp == 1 || warp == 3) {
-        // ---------------- MMA issuers: warp 1 even groups, warp 3 odd groups.
+        // ---------------- MMA issuers: warp 1 even steps, warp 3 odd steps.
         // Issuing a tensor-core instruction occupies the issuing warp's
         // scheduler for tens of cycles; two issuers on two schedulers halve
         // what the epilogue and dequant warps sharing them lose, and
         // consecutive groups' MMA chains (different P buffers) interleave.
         bool ok = true;
         const uint32_t idesc = idesc_bf16(BM, BN);
-        for (int g = warp >> 1; g < G; g += 2) {
-            const int s = g % NS, pb = g % NP;
-            if (!(ok = mbar_wait_warp(&go[s], (g / NS) & 1, args.status))) break;
+        for (int gi = warp >> 1; gi < steps; gi += 2) {
+            const int s = gi % NS, pb = gi % NP;
+            if (!(ok = mbar_wait_warp(&go[s], (gi / NS) & 1, args.status))) break;
             tc_fence_after();
             const uint32_t d = tmem + P_COL + pb * BN;
-            const uint32_t a = tmem + A_COL + (g % NA) * 32;
+            const uint32_t a = tmem + A_COL + (gi % NA) * 32;
             const uint32_t b0 = smem_u32(xs + s * X_STAGE);
             // one elected lane per instruction: measured cheaper to issue than
             // one elected block of four
@@ -287,83 +311,86 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         if (!ok && lane == 0) *abort_flag = 1;
     } else if (warp >= DQ0 && warp < EPI0) {
         // ---------------- dequant: thread = weight row r of the block; groups
-        // (2j, 2j+1) per iteration, so that one weight wait, one stage wait
-        // and one tensor-memory store wait serve two groups and the two
-        // decodes overlap
+        // (2j, 2j+1) of a tile per iteration, so that one weight wait, one
+        // stage wait and one tensor-memory store wait serve two groups and the
+        // two decodes overlap
         const int q = warp & 3;                   // TMEM lane quarter
         const int r = q * 32 + lane;
-        const int tile = r >> 4, i = r & 15, gi = i & 7, half = i >> 3;
-        const int soff = scale_off(codec) + tile * 32 + gi * 4 + half * 2;
+        const int tile = r >> 4, i = r & 15, gi_ = i & 7, half = i >> 3;
+        const int soff = scale_off(codec) + tile * 32 + gi_ * 4 + half * 2;
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         bool ok = true;
-        for (int j = 0; j < (G + 1) / 2; ++j) {
-            const int g0 = 2 * j;
-            const bool two = g0 + 1 < G;
-            const int wsl = j % NWP;
-            if (!(ok = mbar_wait_warp(&w_full[wsl], (j / NWP) & 1, args.status))) break;
-            uint32_t wd[2][8], hw[2][4];
+        int jp = 0;                                   // weight stages used so far
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
+                const int g0 = it * G + 2 * j;        // step of the pair's first group
+                const bool two = 2 * j + 1 < G;
+                const int wsl = jp % NWP;
+                if (!(ok = mbar_wait_warp(&w_full[wsl], (jp / NWP) & 1, args.status))) break;
+                uint32_t wd[2][8], hw[2][4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const uint8_t *u = ws + wsl * 2 * UNIT5 + e * UB;
-                if (e == 0 || two) {
+                for (int e = 0; e < 2; ++e) {
+                    const uint8_t *u = ws + wsl * 2 * UNIT5 + e * UB;
+                    if (e == 0 || two) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi_ + c) * 16 + 8 * half);
+                            wd[e][2 * c] = v.x;
+                            wd[e][2 * c + 1] = v.y;
+                            hw[e][c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi_ + c) * 4) : 0u;
+                        }
+                        // the epilogue of step g0 + e reads this row's scale from the ring
+                        sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) { wd[e][2 * c] = wd[e][2 * c + 1] = 0u; hw[e][c] = 0u; }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[wsl]);
+                // decode to 32 bf16x2 words per group in natural k order: word m = (k 2m, 2m+1)
+                uint32_t av[2][32];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi + c) * 16 + 8 * half);
-                        wd[e][2 * c] = v.x;
-                        wd[e][2 * c + 1] = v.y;
-                        hw[e][c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi + c) * 4) : 0u;
-                    }
-                    // the epilogue of group g0 + e reads this row's scale from the ring
-                    sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
-                } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) { wd[e][2 * c] = wd[e][2 * c + 1] = 0u; hw[e][c] = 0u; }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&w_empty[wsl]);
-            // decode to 32 bf16x2 words per group in natural k order: word m = (k 2m, 2m+1)
-            uint32_t av[2][32];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t w = wd[e][2 * c + h];
-                        uint32_t *o = av[e] + 8 * c + 4 * h;
-                        if (CODEC == 4) {
-                            o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
-                        } else {
-                            // this row's words in the lane's high word: m = 2*half + h
-                            const uint32_t hh = hw[e][c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
-                            o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
-                            o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t w = wd[e][2 * c + h];
+                            uint32_t *o = av[e] + 8 * c + 4 * h;
+                            if (CODEC == 4) {
+                                o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                            } else {
+                                // this row's words in the lane's high word: m = 2*half + h
+                                const uint32_t hh = hw[e][c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
+                                o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                                o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                            }
                         }
                     }
                 }
-            }
-            // the A stages of both groups are free once the MMAs of groups
-            // g0 - NA and g0 + 1 - NA have completed
-            if (two && g0 + 1 >= NA) {
-                // (g0 >= NA too: both are even)
+                // the A stages of both groups are free once the MMAs of steps
+                // g0 - NA and g0 + 1 - NA have completed
                 const int h0 = g0 - NA, h1 = g0 + 1 - NA;
-                ok = __all_sync(0xffffffffu, mbar_wait2(&done[h0 % NS], (h0 / NS) & 1, &done[h1 % NS], (h1 / NS) & 1,
-                                                        args.status));
-            } else if (g0 >= NA) {
-                const int h0 = g0 - NA;
-                ok = mbar_wait_warp(&done[h0 % NS], (h0 / NS) & 1, args.status);
-            }
-            if (!ok) break;
-            tc_fence_after();
-            tc_st32(tmem + tlane + A_COL + (g0 % NA) * 32, av[0]);
-            if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NA) * 32, av[1]);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&go[g0 % NS]);
-                if (two) mbar_arrive(&go[(g0 + 1) % NS]);
+                if (two && h1 >= 0 && h0 >= 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait2(&done[h0 % NS], (h0 / NS) & 1, &done[h1 % NS], (h1 / NS) & 1,
+                                                            args.status));
+                } else if (h0 >= 0) {
+                    ok = mbar_wait_warp(&done[h0 % NS], (h0 / NS) & 1, args.status);
+                } else if (two && h1 >= 0) {
+                    ok = mbar_wait_warp(&done[h1 % NS], (h1 / NS) & 1, args.status);
+                }
+                if (!ok) break;
+                tc_fence_after();
+                tc_st32(tmem + tlane + A_COL + (g0 % NA) * 32, av[0]);
+                if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NA) * 32, av[1]);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&go[g0 % NS]);
+                    if (two) mbar_arrive(&go[(g0 + 1) % NS]);
+                }
             }
         }
         if (!ok && lane == 0) *abort_flag = 1;
@@ -371,53 +398,61 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         // ---------------- epilogue: thread = row r, columns [64*hc, 64*hc + 64)
         const int q = warp & 3, hc = (warp - EPI0) >> 2;
         const int r = q * 32 + lane;
-        // the first NP groups find their P buffer empty
+        // the first NP steps find their P buffer empty
         if (lane == 0)
-            for (int g = 0; g < NP && g < G; ++g) mbar_arrive(&go[g]);
-        float2 acc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
+            for (int g = 0; g < NP && g < steps; ++g) mbar_arrive(&go[g]);
         bool ok = true;
-        for (int g = 0; g < G; ++g) {
-            const int ps = g % NP;
-            // polled: the epilogue gates the MMAs of group g + NP
-            if (!(ok = mbar_spin_warp(&done[g % NS], (g / NS) & 1, args.status))) break;
-            tc_fence_after();
-            const float s = sc_ring[(g % SC_RING) * BM + r];
-            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
-            // both loads in flight before one wait: the P buffer is released one
-            // load latency after it filled
-            uint32_t v0[32], v1[32];
-            tc_ld32(base, v0);
-            tc_ld32(base + 32, v1);
-            tc_wait_ld();
-            tc_regs_ready(v0);
-            tc_regs_ready(v1);
-            tc_fence_before();
-            __syncwarp();
-            // P buffer ps is free for group g + NP
-            if (lane == 0 && g + NP < G) mbar_arrive(&go[(g + NP) % NS]);
-            // packed f32x2 FMAs: half the instructions of scalar ones
-            const float2 s2 = make_float2(s, s);
+        int gi = 0;
+        for (int it = 0; it < my_tiles && ok; ++it) {
+            float2 acc[32];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
+            for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
+            for (int k = 0; k < G; ++k, ++gi) {
+                const int ps = gi % NP;
+                // polled: the epilogue gates the MMAs of step gi + NP
+                if (!(ok = mbar_spin_warp(&done[gi % NS], (gi / NS) & 1, args.status))) break;
+                tc_fence_after();
+                const float s = sc_ring[(gi % SC_RING) * BM + r];
+                const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
+                // both loads in flight before one wait: the P buffer is released
+                // one load latency after it filled
+                uint32_t v0[32], v1[32];
+                tc_ld32(base, v0);
+                tc_ld32(base + 32, v1);
+                tc_wait_ld();
+                tc_regs_ready(v0);
+                tc_regs_ready(v1);
+                tc_fence_before();
+                __syncwarp();
+                // P buffer ps is free for step gi + NP
+                if (lane == 0 && gi + NP < steps) mbar_arrive(&go[(gi + NP) % NS]);
+                // packed f32x2 FMAs: half the instructions of scalar ones
+                const float2 s2 = make_float2(s, s);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
-        }
-        if (!ok && lane == 0) *abort_flag = 1;
-        // ---- write Y[t][n] (consecutive lanes = consecutive rows n)
-        const int n = blk * BM + r;
-        if (ok && n < P.N) {
-            const int t0 = tt * BN + hc * 64;
+                for (int j = 0; j < 16; ++j)
+                    acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = t0 + 2 * j;
-                if (t < T) P.Y[(size_t)t * P.N + n] = acc[j].x;
-                if (t + 1 < T) P.Y[(size_t)(t + 1) * P.N + n] = acc[j].y;
+                for (int j = 0; j < 16; ++j)
+                    acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
+            }
+            if (!ok) break;
+            // ---- write this tile's Y[t][n] (consecutive lanes = consecutive rows
+            // n) while the MMAs of the next tile run
+            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
+            const int n = tr.blk * BM + r;
+            if (n < tr.P->N) {
+                float *Y = tr.P->Y;
+                const int N = tr.P->N;
+                const int t0 = tr.tt * BN + hc * 64;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int t = t0 + 2 * j;
+                    if (t < T) Y[(size_t)t * N + n] = acc[j].x;
+                    if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[j].y;
+                }
             }
         }
+        if (!ok && lane == 0) *abort_flag = 1;
     }
 
     // ---- every role is done with tensor memory: release it
@@ -479,6 +514,7 @@ template <int CODEC>
 static cudaError_t launch_codec(const WideParent *parents, int np, const CUtensorMap &xmap, int T, int K,
                                 unsigned int *status, cudaStream_t stream) {
     static bool attr_set[64] = {};
+    static int sms[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -486,26 +522,31 @@ static cudaError_t launch_codec(const WideParent *parents, int np, const CUtenso
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(wide_kernel<CODEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::Smem::BYTES);
         if (e != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     WideArgs a;
     memset(&a, 0, sizeof a);
     const int ntt = (T + wide::BN - 1) / wide::BN;
-    int grid = 0;
+    int tiles = 0;
     for (int i = 0; i < np; ++i) {
         if (parents[i].codec != CODEC) continue;
         WideParent &d = a.p[a.nparents++];
         d = parents[i];
-        d.cta_begin = grid;
+        d.cta_begin = tiles;
         d.nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
-        grid += d.nblocks * ntt;
+        tiles += d.nblocks * ntt;
     }
-    if (grid == 0) return cudaSuccess;
+    if (tiles == 0) return cudaSuccess;
     a.T = T;
     a.K = K;
     a.G = K / GROUP;
     a.ntt = ntt;
+    a.ntiles = tiles;
     a.status = status;
+    // persistent: one CTA per SM (its shared memory allows no more), each
+    // taking the tiles blockIdx.x, blockIdx.x + grid, ...
+    const int grid = tiles < sms[dev] ? tiles : sms[dev];
     wide_kernel<CODEC><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
     return cudaGetLastError();
 }

@@ -48,6 +48,10 @@ def _bind(lib):
     lib.qgemm_oracle_dequant.restype = i32
     lib.qgemm_oracle_gemm.argtypes = [i32, i32, i32, i32, ptr, ptr, ptr, ptr, ptr]
     lib.qgemm_oracle_gemm.restype = i32
+    lib.qgemm_oracle_linear_add.argtypes = [i32, i32, i32, i32, ptr, ptr, ptr, ptr, ptr, ptr]
+    lib.qgemm_oracle_linear_add.restype = i32
+    lib.qgemm_oracle_swiglu.argtypes = [i32, ptr, ptr, ptr]
+    lib.qgemm_oracle_swiglu.restype = i32
     return lib
 
 
@@ -114,3 +118,41 @@ def gemm_parent(parent: dict, x_bf16: np.ndarray, lib=None):
     """Oracle on one weight matrix as drawn by the input generator."""
     return gemm(parent["bits"], parent["packed"], parent["scales"], x_bf16,
                 parent["N"], parent["K"], lib=lib)
+
+
+def linear_add(bits: int, packed: np.ndarray, scales: np.ndarray, x_bf16: np.ndarray, R: np.ndarray,
+               N: int, K: int, lib=None):
+    """(Y, A) of Y = R + X . deq(W)^T; R fp32 [T, N]."""
+    lib = lib or load()
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    T = x.shape[0]
+    R = np.ascontiguousarray(R, dtype=np.float32)
+    assert x.shape == (T, K) and R.shape == (T, N), (x.shape, R.shape, T, N, K)
+    Y = np.zeros((T, N), np.float64)
+    A = np.zeros((T, N), np.float64)
+    if lib.qgemm_oracle_linear_add(bits, N, K, T, _p(packed), _p(scales), _p(x), _p(R), _p(Y), _p(A)) != 0:
+        raise ValueError("oracle linear_add: bad arguments")
+    return Y, A
+
+
+def swiglu(g: np.ndarray, u: np.ndarray, lib=None) -> np.ndarray:
+    """silu(g) * u elementwise in fp64 (g, u same shape)."""
+    lib = lib or load()
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    assert g.shape == u.shape
+    out = np.zeros(g.shape, np.float64)
+    if lib.qgemm_oracle_swiglu(g.size, _p(g), _p(u), _p(out)) != 0:
+        raise ValueError("oracle swiglu: bad arguments")
+    return out
+
+
+def swiglu_pair(gate: dict, up: dict, x_bf16: np.ndarray, lib=None):
+    """(out, g, u, A_g, A_u): the SwiGLU of a gate/up pair of weight matrices
+    as drawn by the input generator, with the plain results and their sums of
+    |products| (for the tolerance)."""
+    g, Ag = gemm_parent(gate, x_bf16, lib=lib)
+    u, Au = gemm_parent(up, x_bf16, lib=lib)
+    return swiglu(g, u, lib=lib), g, u, Ag, Au

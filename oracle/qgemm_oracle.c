@@ -36,6 +36,15 @@
  * itself requires K % 64 == 0; the oracle accepts any K so that tiny
  * brute-force cases can run).
  * X: bf16 bit patterns, row-major [T][K].  Y, A: fp64, row-major [T][N].
+ *
+ * The two fused outputs of the pages' projections ("ninfer-3080
+ * docs/performance.md": LinearAdd on the attention o_proj and GDN out_proj,
+ * the SwiGLU gate/up pair on the MLP) are written out the same way:
+ *
+ *     linear add:  Y[t][n] = R[t][n] + sum_k x[t][k] * w[n][k]
+ *     SwiGLU:      out[t][f] = silu(g[t][f]) * u[t][f],  silu(z) = z / (1 + e^-z)
+ *
+ * with g and u the plain results of the gate and the up matrix.
  */
 #include <math.h>
 #include <stddef.h>
@@ -167,5 +176,36 @@ int qgemm_oracle_gemm(int bits, int N, int K, int T, const uint8_t *packed,
         }
     }
     free(w);
+    return 0;
+}
+
+/*
+ * Y[t][n] = R[t][n] + (the gemm above), A[t][n] = |R[t][n]| + (its sum of
+ * |products|).  R is fp32 (the library's residual type), read exactly.
+ */
+int qgemm_oracle_linear_add(int bits, int N, int K, int T, const uint8_t *packed,
+                            const uint16_t *scales, const uint16_t *X, const float *R,
+                            double *Y, double *A)
+{
+    if (!R)
+        return -1;
+    int st = qgemm_oracle_gemm(bits, N, K, T, packed, scales, X, Y, A);
+    if (st != 0)
+        return st;
+    for (size_t i = 0; i < (size_t)T * (size_t)N; ++i) {
+        Y[i] = (double)R[i] + Y[i];
+        if (A)
+            A[i] = fabs((double)R[i]) + A[i];
+    }
+    return 0;
+}
+
+/* out[i] = silu(g[i]) * u[i] with silu(z) = z / (1 + exp(-z)), in fp64. */
+int qgemm_oracle_swiglu(int n, const double *g, const double *u, double *out)
+{
+    if (n < 0 || (n > 0 && (!g || !u || !out)))
+        return -1;
+    for (int i = 0; i < n; ++i)
+        out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
     return 0;
 }

@@ -218,9 +218,60 @@ def pin_column_independence(lib):
         assert np.array_equal(Yt[0], Y[t])
 
 
+def pin_swiglu(lib):
+    # closed forms: sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 exactly, so
+    # silu(+-ln 3) = +-(3/4 or 1/4) ln 3; silu(0) = 0; silu(z) -> z for large z
+    l3 = np.log(3.0)
+    g = np.array([0.0, l3, -l3, 40.0, -40.0, 1.5])
+    u = np.array([7.0, 2.0, 2.0, 0.5, 1.0, -3.0])
+    out = oracle.swiglu(g, u, lib=lib)
+    assert out[0] == 0.0
+    assert abs(out[1] - 1.5 * l3) <= 4 * U * 1.5 * l3
+    assert abs(out[2] + 0.5 * l3) <= 4 * U * 0.5 * l3
+    assert abs(out[3] - 20.0) <= 1e-15 * 20.0
+    assert abs(out[4]) < 1e-15
+    # against scipy's logistic function (a library routine) on random inputs
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(5)
+    g = rng.uniform(-30, 30, 257)
+    u = rng.normal(0, 3, 257)
+    ref = g * special.expit(g) * u
+    assert np.allclose(oracle.swiglu(g, u, lib=lib), ref, rtol=1e-13, atol=1e-300)
+
+
+def pin_linear_add(lib):
+    N, K, T = 9, 192, 3
+    w, x = small_case(41, N, K, T, 4)
+    rng = np.random.default_rng(41)
+    R = rng.normal(0, 4, (T, N)).astype(np.float32)
+    Rd = R.astype(np.float64)
+    # zero scales: the product term vanishes and Y is R itself, A is |R|
+    zero = np.zeros_like(w["scales"])
+    Y0, A0 = oracle.linear_add(4, w["packed"], zero, x, R, N, K, lib=lib)
+    assert np.array_equal(Y0, Rd) and np.array_equal(A0, np.abs(Rd))
+    # zero residual: the plain result
+    Yg, Ag = oracle.gemm(4, w["packed"], w["scales"], x, N, K, lib=lib)
+    Yz, Az = oracle.linear_add(4, w["packed"], w["scales"], x, np.zeros((T, N), np.float32), N, K, lib=lib)
+    assert np.array_equal(Yz, Yg) and np.array_equal(Az, Ag)
+    # integer-valued weights and activations: every sum is exact, so Y = R + Y0 exactly
+    codes = synth.uniform_codes(41, 3, N, K, 4)
+    ones = np.full((N, K // 64), 0x3C00, np.uint16)                  # fp16 1.0
+    xi = synth.fp64_to_bf16_bits(rng.integers(-3, 4, (T, K)).astype(np.float64))
+    Ri = rng.integers(-1000, 1000, (T, N)).astype(np.float32)
+    Yi, _ = oracle.linear_add(4, synth.pack_canonical(codes, 4), ones, xi, Ri, N, K, lib=lib)
+    exact = Ri.astype(np.int64) + rng_free_dot(xi, codes)
+    assert np.array_equal(Yi, exact.astype(np.float64))
+
+
+def rng_free_dot(x_bits, codes):
+    """Integer X . codes^T for integer-valued bf16 activations (exact, in int64)."""
+    xv = bf16_values(x_bits).astype(np.int64)
+    return xv @ codes.astype(np.int64).T
+
+
 PINS = [pin_golden, pin_exact_rational, pin_bruteforce_int4, pin_bruteforce_int5, pin_numpy_matmul,
         pin_linearity_exact, pin_identity_and_permutation, pin_scaling_and_negation,
-        pin_int5_contains_int4, pin_column_independence]
+        pin_int5_contains_int4, pin_column_independence, pin_swiglu, pin_linear_add]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -245,6 +296,11 @@ MUTANTS = {
     "half_bias": ("expo - 25);", "expo - 24);"),
     "half_subnormal": ("ldexp((double)mant, -24);", "ldexp((double)mant, -25);"),
     "group_width": ("#define ORACLE_GROUP 64", "#define ORACLE_GROUP 128"),
+    "silu_sign": ("out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "out[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
+    "silu_gate_up_swapped": ("out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];",
+                             "out[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
+    "residual_dropped": ("Y[i] = (double)R[i] + Y[i];", "Y[i] = Y[i];"),
+    "residual_abs": ("A[i] = fabs((double)R[i]) + A[i];", "A[i] = (double)R[i] + A[i];"),
 }
 
 

@@ -33,12 +33,19 @@ QGEMM_ERR_UNSUPPORTED = 8
 QGEMM_INT4 = 4
 QGEMM_INT5 = 5
 
+QGEMM_EPILOGUE_STORE = 0
+QGEMM_EPILOGUE_ADD = 1
+QGEMM_EPILOGUE_SWIGLU = 2
+QGEMM_OUT_F32 = 0
+QGEMM_OUT_BF16 = 1
+
 # every symbol include/qgemm.h declares
 EXPORTS = [
     "qgemm_status_string", "qgemm_packed_bytes", "qgemm_pack_weights", "qgemm_plan",
     "qgemm_plan_workspace_bytes", "qgemm_plan_bind", "qgemm_run", "qgemm_run_multi",
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
-    "qgemm_device_status", "qgemm_plan_set_pdl",
+    "qgemm_device_status", "qgemm_plan_set_pdl", "qgemm_pair_packed_bytes", "qgemm_pack_pair",
+    "qgemm_plan_set_epilogue", "qgemm_run_ex",
 ]
 
 _lock = threading.Lock()
@@ -69,6 +76,10 @@ def _declare(lib):
         "qgemm_launch_count": ([], u64),
         "qgemm_device_status": ([vp, i32], i32),
         "qgemm_plan_set_pdl": ([vp, i32], i32),
+        "qgemm_pair_packed_bytes": ([i32, i32, i32], sz),
+        "qgemm_pack_pair": ([i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
+        "qgemm_plan_set_epilogue": ([vp, i32, i32], i32),
+        "qgemm_run_ex": ([vp, vp, i32, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -156,6 +167,24 @@ def qgemm_plan_destroy(plan) -> int:
     return load().qgemm_plan_destroy(plan)
 
 
+def qgemm_pair_packed_bytes(F: int, K: int, codec: int) -> int:
+    return load().qgemm_pair_packed_bytes(F, K, codec)
+
+
+def qgemm_pack_pair(codec, F, K, gate_codes_dev, gate_scales_dev, up_codes_dev, up_scales_dev, packed_dev,
+                    stream=None) -> int:
+    return load().qgemm_pack_pair(codec, F, K, _ptr(gate_codes_dev), _ptr(gate_scales_dev), _ptr(up_codes_dev),
+                                  _ptr(up_scales_dev), _ptr(packed_dev), _stream(stream))
+
+
+def qgemm_plan_set_epilogue(plan, epilogue: int, out: int = QGEMM_OUT_F32) -> int:
+    return load().qgemm_plan_set_epilogue(plan, epilogue, out)
+
+
+def qgemm_run_ex(plan, X, T: int, R, Y, stream=None) -> int:
+    return load().qgemm_run_ex(plan, _ptr(X), T, _ptr(R), _ptr(Y), _stream(stream))
+
+
 def qgemm_plan_set_pdl(plan, enable: bool) -> int:
     return load().qgemm_plan_set_pdl(plan, 1 if enable else 0)
 
@@ -181,7 +210,15 @@ def check(status: int, what: str = "") -> None:
         raise QgemmError(status, what)
 
 
-# ------------------------------------------------------------ convenience holder
+# ------------------------------------------------------------ convenience holders
+
+def _to_dev(a, dtype, dev):
+    import numpy as np
+    import torch
+    if isinstance(a, np.ndarray):
+        a = torch.from_numpy(np.ascontiguousarray(a).view(dtype))
+    return a.to(dev).contiguous()
+
 
 class GroupwiseWeights:
     """One packed weight matrix bound to a plan (device memory from torch).
@@ -192,26 +229,27 @@ class GroupwiseWeights:
     """
 
     def __init__(self, codec: int, N: int, K: int, codes_canonical, scales_fp16, T_max: int,
-                 device="cuda", stream=None):
+                 device="cuda", stream=None, epilogue: int = QGEMM_EPILOGUE_STORE, out: int = QGEMM_OUT_F32):
         import numpy as np
         import torch
         self.codec, self.N, self.K, self.T_max = codec, N, K, T_max
+        self.epilogue, self.out = epilogue, out
         dev = torch.device(device)
-
-        def to_dev(a, dtype):
-            if isinstance(a, np.ndarray):
-                a = torch.from_numpy(np.ascontiguousarray(a).view(dtype))
-            return a.to(dev).contiguous()
-
-        codes = to_dev(codes_canonical, np.uint8)
-        scales = to_dev(scales_fp16, np.int16)
+        codes = _to_dev(codes_canonical, np.uint8, dev)
+        scales = _to_dev(scales_fp16, np.int16, dev)
         nbytes = qgemm_packed_bytes(N, K, codec)
         if nbytes == 0:
             raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_packed_bytes")
         self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         check(qgemm_pack_weights(codec, N, K, codes, scales, self.packed, stream), "qgemm_pack_weights")
-        st, self.plan = qgemm_plan(N, K, codec, T_max)
+        self._make_plan(dev)
+
+    def _make_plan(self, dev):
+        import torch
+        st, self.plan = qgemm_plan(self.N, self.K, self.codec, self.T_max)
         check(st, "qgemm_plan")
+        if (self.epilogue, self.out) != (QGEMM_EPILOGUE_STORE, QGEMM_OUT_F32):
+            check(qgemm_plan_set_epilogue(self.plan, self.epilogue, self.out), "qgemm_plan_set_epilogue")
         wsb = qgemm_plan_workspace_bytes(self.plan)
         self.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
         check(qgemm_plan_bind(self.plan, self.packed, self.workspace, self.workspace.numel()), "qgemm_plan_bind")
@@ -219,13 +257,18 @@ class GroupwiseWeights:
     def route(self, T: int) -> str:
         return qgemm_route_name(qgemm_plan_route(self.plan, T))
 
-    def run(self, X, Y=None, stream=None):
-        """Y[T, N] fp32 = X[T, K] (bf16) . deq(W)^T."""
+    def run(self, X, Y=None, stream=None, R=None):
+        """Y = epilogue(X[T, K] (bf16) . deq(W)^T): fp32 or bf16 [T, N] ([T, F]
+        for a SwiGLU pair); R is the fp32 [T, N] residual of an ADD plan."""
         import torch
         T = X.shape[0]
         if Y is None:
-            Y = torch.empty((T, self.N), dtype=torch.float32, device=X.device)
-        check(qgemm_run(self.plan, X, T, Y, stream), "qgemm_run")
+            dtype = torch.bfloat16 if self.out == QGEMM_OUT_BF16 else torch.float32
+            Y = torch.empty((T, self.N), dtype=dtype, device=X.device)
+        if (self.epilogue, self.out) == (QGEMM_EPILOGUE_STORE, QGEMM_OUT_F32) and R is None:
+            check(qgemm_run(self.plan, X, T, Y, stream), "qgemm_run")
+        else:
+            check(qgemm_run_ex(self.plan, X, T, R, Y, stream), "qgemm_run_ex")
         return Y
 
     def close(self):
@@ -248,3 +291,24 @@ def run_multi(weights, X, Ys=None, stream=None):
         Ys = [torch.empty((T, w.N), dtype=torch.float32, device=X.device) for w in weights]
     check(qgemm_run_multi([w.plan for w in weights], X, T, Ys, stream), "qgemm_run_multi")
     return Ys
+
+
+class SwiGLUPair(GroupwiseWeights):
+    """The gate and up matrices of an MLP (F x K each, same codec) packed as one
+    pair; ``run(X)`` returns silu(X . G^T) * (X . U^T), [T, F]."""
+
+    def __init__(self, codec: int, F: int, K: int, gate_codes, gate_scales, up_codes, up_scales, T_max: int,
+                 device="cuda", stream=None, out: int = QGEMM_OUT_F32):
+        import numpy as np
+        import torch
+        self.codec, self.N, self.K, self.T_max = codec, F, K, T_max
+        self.epilogue, self.out = QGEMM_EPILOGUE_SWIGLU, out
+        dev = torch.device(device)
+        nbytes = qgemm_pair_packed_bytes(F, K, codec)
+        if nbytes == 0:
+            raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_pair_packed_bytes")
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        check(qgemm_pack_pair(codec, F, K, _to_dev(gate_codes, np.uint8, dev), _to_dev(gate_scales, np.int16, dev),
+                              _to_dev(up_codes, np.uint8, dev), _to_dev(up_scales, np.int16, dev), self.packed,
+                              stream), "qgemm_pack_pair")
+        self._make_plan(dev)

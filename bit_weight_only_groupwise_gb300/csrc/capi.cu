@@ -13,6 +13,8 @@ namespace qg {
 cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16_t *scales, void *out,
                         cudaStream_t stream);
 cudaError_t launch_fence(cudaStream_t stream);
+cudaError_t launch_pack_pair(int codec, int F, int K, const void *gate, const uint16_t *gate_scales,
+                             const void *up, const uint16_t *up_scales, void *out, cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
 int skinny_line_groups(int G, int nj_pref);
 cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream);
@@ -65,6 +67,8 @@ static int choose_route(int T) {
 
 struct qgemm_plan_s {
     int N, K, codec, T_max;
+    int rows;              // packed rows: N, or pair_rows(N) for a SwiGLU pair
+    int epi, out;          // qgemm_epilogue, qgemm_out
     int G, NB, UB;
     int sms;
     bool pdl;              // launch with programmatic dependent launch
@@ -161,6 +165,9 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     p->K = K;
     p->codec = codec;
     p->T_max = T_max;
+    p->rows = N;
+    p->epi = QGEMM_EPILOGUE_STORE;
+    p->out = QGEMM_OUT_F32;
     p->G = K / GROUP;
     p->NB = (N + BLOCK_ROWS - 1) / BLOCK_ROWS;
     p->UB = unit_bytes(codec);
@@ -188,6 +195,39 @@ qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev, void *wo
 
 qgemm_status qgemm_plan_destroy(qgemm_plan_t plan) {
     delete plan;
+    return QGEMM_OK;
+}
+
+size_t qgemm_pair_packed_bytes(int F, int K, qgemm_codec codec) {
+    if (F < 1 || F > (1 << 29)) return 0;
+    return qgemm_packed_bytes(pair_rows(F), K, codec);
+}
+
+qgemm_status qgemm_pack_pair(qgemm_codec codec, int F, int K, const void *gate_codes_dev,
+                             const uint16_t *gate_scales_dev, const void *up_codes_dev,
+                             const uint16_t *up_scales_dev, void *packed_dev, qgemm_stream_t stream) {
+    if (!valid_codec(codec)) return QGEMM_ERR_INVALID_ARG;
+    if (F < 1 || F > (1 << 29) || K < GROUP || K % GROUP) return QGEMM_ERR_SHAPE;
+    if (!gate_codes_dev || !gate_scales_dev || !up_codes_dev || !up_scales_dev || !packed_dev)
+        return QGEMM_ERR_INVALID_ARG;
+    if (!aligned16(packed_dev)) return QGEMM_ERR_ALIGNMENT;
+    if (launch_pack_pair(codec, F, K, gate_codes_dev, gate_scales_dev, up_codes_dev, up_scales_dev, packed_dev,
+                         (cudaStream_t)stream) != cudaSuccess)
+        return QGEMM_ERR_CUDA;
+    if (launch_fence((cudaStream_t)stream) != cudaSuccess) return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(2);
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue, qgemm_out out) {
+    if (!plan || plan->bound) return QGEMM_ERR_INVALID_ARG;
+    if (epilogue != QGEMM_EPILOGUE_STORE && epilogue != QGEMM_EPILOGUE_ADD && epilogue != QGEMM_EPILOGUE_SWIGLU)
+        return QGEMM_ERR_INVALID_ARG;
+    if (out != QGEMM_OUT_F32 && out != QGEMM_OUT_BF16) return QGEMM_ERR_INVALID_ARG;
+    plan->epi = epilogue;
+    plan->out = out;
+    plan->rows = epilogue == QGEMM_EPILOGUE_SWIGLU ? pair_rows(plan->N) : plan->N;
+    plan->NB = (plan->rows + BLOCK_ROWS - 1) / BLOCK_ROWS;
     return QGEMM_OK;
 }
 
@@ -228,12 +268,16 @@ qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear) {
 
 // ---------------------------------------------------------------- runs
 
-static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, float *Y, int cta_begin) {
+static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, void *Y, const float *R, int cta_begin) {
     sp.packed = p->packed;
     sp.Y = Y;
-    sp.N = p->N;
+    sp.R = R;
+    sp.N = p->rows;
     sp.codec = p->codec;
     sp.cta_begin = cta_begin;
+    sp.ncols = p->N;
+    sp.epi = p->epi;
+    sp.ybf16 = p->out == QGEMM_OUT_BF16;
 }
 
 // Tuning knob read once from the environment, for sweeps only:
@@ -247,7 +291,7 @@ static int env_int(const char *name, int dflt) {
 
 // One or more parents over the same X in one launch of the route T selects.
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
-                                float *const *Ys, cudaStream_t stream) {
+                                void *const *Ys, const float *R, cudaStream_t stream) {
     static const int kw = env_int("QGEMM_SKINNY_WARPS", 8);
     static const int line = env_int("QGEMM_SKINNY_LINE", 8);
     const int route = choose_route(T);
@@ -261,8 +305,12 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
         for (int i = 0; i < np; ++i) {
             wp[i].packed = plans[i]->packed;
             wp[i].Y = Ys[i];
-            wp[i].N = plans[i]->N;
+            wp[i].R = R;
+            wp[i].N = plans[i]->rows;
             wp[i].codec = plans[i]->codec;
+            wp[i].ncols = plans[i]->N;
+            wp[i].epi = plans[i]->epi;
+            wp[i].ybf16 = plans[i]->out == QGEMM_OUT_BF16;
         }
         int launches = 0;
         if (launch_wide(wp, np, X, T, K, status, stream, &launches) != cudaSuccess) return QGEMM_ERR_CUDA;
@@ -275,8 +323,8 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     memset(&a, 0, sizeof a);
     int grid = 0;
     for (int i = 0; i < np; ++i) {
-        fill_parent(a.p[i], plans[i], Ys[i], grid);
-        grid += (plans[i]->N + 15) / 16;
+        fill_parent(a.p[i], plans[i], Ys[i], R, grid);
+        grid += (plans[i]->rows + 15) / 16;
     }
     a.nparents = np;
     a.status = status;
@@ -292,7 +340,7 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     return QGEMM_OK;
 }
 
-static qgemm_status check_run(const qgemm_plan_s *p, const void *X, int T, const float *Y) {
+static qgemm_status check_run(const qgemm_plan_s *p, const void *X, int T, const void *Y) {
     if (!p || !p->bound) return QGEMM_ERR_INVALID_ARG;
     if (T < 0) return QGEMM_ERR_INVALID_ARG;
     if (T > p->T_max) return QGEMM_ERR_T_OUT_OF_DOMAIN;
@@ -303,19 +351,36 @@ static qgemm_status check_run(const qgemm_plan_s *p, const void *X, int T, const
     return QGEMM_OK;
 }
 
+static bool plain_output(const qgemm_plan_s *p) {
+    return p->epi == QGEMM_EPILOGUE_STORE && p->out == QGEMM_OUT_F32;
+}
+
 extern "C" qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_stream_t stream) {
+    if (plan && !plain_output(plan)) return QGEMM_ERR_INVALID_ARG;
     const qgemm_status st = check_run(plan, X, T, Y);
     if (st != QGEMM_OK || T == 0) return st;
     const qgemm_plan_s *plans[1] = {plan};
-    float *Ys[1] = {Y};
-    return run_parents(plans, 1, X, T, Ys, (cudaStream_t)stream);
+    void *Ys[1] = {Y};
+    return run_parents(plans, 1, X, T, Ys, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" qgemm_status qgemm_run_ex(qgemm_plan_t plan, const void *X, int T, const void *R, void *Y,
+                                     qgemm_stream_t stream) {
+    if (!plan) return QGEMM_ERR_INVALID_ARG;
+    if ((plan->epi == QGEMM_EPILOGUE_ADD) != (R != nullptr)) return QGEMM_ERR_INVALID_ARG;
+    const qgemm_status st = check_run(plan, X, T, Y);
+    if (st != QGEMM_OK || T == 0) return st;
+    if (R && !aligned16(R)) return QGEMM_ERR_ALIGNMENT;
+    const qgemm_plan_s *plans[1] = {plan};
+    void *Ys[1] = {Y};
+    return run_parents(plans, 1, X, T, Ys, static_cast<const float *>(R), (cudaStream_t)stream);
 }
 
 extern "C" qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
                                         float *const *Ys, qgemm_stream_t stream) {
     if (!plans || !Ys || n_parents < 1 || n_parents > MAX_PARENTS) return QGEMM_ERR_INVALID_ARG;
     for (int i = 0; i < n_parents; ++i) {
-        if (!plans[i]) return QGEMM_ERR_INVALID_ARG;
+        if (!plans[i] || !plain_output(plans[i])) return QGEMM_ERR_INVALID_ARG;
         if (plans[i]->K != plans[0]->K) return QGEMM_ERR_SHAPE;
         for (int j = 0; j < i; ++j)
             if (plans[j] == plans[i]) return QGEMM_ERR_INVALID_ARG;   // one workspace per parent
@@ -324,6 +389,10 @@ extern "C" qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents
     }
     if (T == 0) return QGEMM_OK;
     const qgemm_plan_s *ps[MAX_PARENTS];
-    for (int i = 0; i < n_parents; ++i) ps[i] = plans[i];
-    return run_parents(ps, n_parents, X, T, Ys, (cudaStream_t)stream);
+    void *ys[MAX_PARENTS];
+    for (int i = 0; i < n_parents; ++i) {
+        ps[i] = plans[i];
+        ys[i] = Ys[i];
+    }
+    return run_parents(ps, n_parents, X, T, ys, nullptr, (cudaStream_t)stream);
 }

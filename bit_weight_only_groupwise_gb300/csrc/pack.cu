@@ -2,12 +2,31 @@
 // described in qgemm_internal.cuh.  One CTA per unit (block b, group grp), one
 // thread per (tile, lane): each thread builds one lane's 16-byte code chunk,
 // its int5 high word, and (lanes with c == 0) one scale pair.
+//
+// A SwiGLU pair (gate and up, F rows each) is packed as one matrix of
+// pair_rows(F) rows whose 16-row tiles hold 8 gate rows and then the same 8
+// up rows: packed row 16 b + 8 h + i is row 8 b + i of the gate (h = 0) or of
+// the up matrix (h = 1), so that the lane owning rows g and g + 8 of a tile
+// holds the gate and the up value of one output.
 #include "qgemm_internal.cuh"
 
 namespace qg {
 
+// Source of packed row `row`: the matrix (0: the plain or gate matrix, 1: the
+// up matrix) and its row, or row -1 for padding.
+struct SrcRow { int which, row; };
+
+__device__ __forceinline__ SrcRow src_row(int row, int N, int F) {
+    if (F == 0) return {0, row < N ? row : -1};
+    const int f = (row >> 4) * 8 + (row & 7);
+    return {(row >> 3) & 1, f < F ? f : -1};
+}
+
 __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, const uint8_t *__restrict__ canon,
-                                                   const uint16_t *__restrict__ scales, uint8_t *__restrict__ out) {
+                                                   const uint16_t *__restrict__ scales,
+                                                   const uint8_t *__restrict__ canon_up,
+                                                   const uint16_t *__restrict__ scales_up, int F,
+                                                   uint8_t *__restrict__ out) {
     const int G = K / GROUP;
     const int unit = blockIdx.x;            // b * G + grp
     const int b = unit / G, grp = unit % G;
@@ -19,14 +38,16 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
     uint32_t words[4] = {0, 0, 0, 0};
     uint32_t hi = 0;
     for (int half = 0; half < 2; ++half) {          // rows r0 and r0 + 8
-        const int row = b * BLOCK_ROWS + 16 * w + g + 8 * half;
+        const SrcRow sr = src_row(b * BLOCK_ROWS + 16 * w + g + 8 * half, N, F);
+        const int row = sr.row;
+        const uint8_t *src = sr.which ? canon_up : canon;
         const int k0 = grp * GROUP + 16 * c;
         for (int j = 0; j < 16; ++j) {
             int ub;                                   // biased code
-            if (row >= N) {
+            if (row < 0) {
                 ub = codec == 5 ? 16 : 8;
             } else if (codec == 4) {
-                const uint8_t byte = canon[(size_t)row * (K / 2) + (k0 + j) / 2];
+                const uint8_t byte = src[(size_t)row * (K / 2) + (k0 + j) / 2];
                 const int nib = ((k0 + j) & 1) ? (byte >> 4) : (byte & 15);
                 ub = nib ^ 8;                         // two's complement nibble -> q + 8
             } else {
@@ -34,7 +55,7 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
                 int v = 0;
                 for (int t = 0; t < 5; ++t) {
                     const size_t p = rowbits + (size_t)5 * (k0 + j) + t;
-                    v |= ((canon[p >> 3] >> (p & 7)) & 1) << t;
+                    v |= ((src[p >> 3] >> (p & 7)) & 1) << t;
                 }
                 ub = v ^ 16;                          // two's complement 5-bit field -> q + 16
             }
@@ -47,9 +68,10 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
     *reinterpret_cast<uint4 *>(u + w * 512 + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
     if (codec == 5) *reinterpret_cast<uint32_t *>(u + NIB_BYTES + w * 128 + lane * 4) = hi;
     if (c == 0) {
-        const int r0 = b * BLOCK_ROWS + 16 * w + g;
-        const uint16_t s0 = r0 < N ? scales[(size_t)r0 * G + grp] : 0;
-        const uint16_t s1 = r0 + 8 < N ? scales[(size_t)(r0 + 8) * G + grp] : 0;
+        const SrcRow a0 = src_row(b * BLOCK_ROWS + 16 * w + g, N, F);
+        const SrcRow a1 = src_row(b * BLOCK_ROWS + 16 * w + g + 8, N, F);
+        const uint16_t s0 = a0.row >= 0 ? (a0.which ? scales_up : scales)[(size_t)a0.row * G + grp] : 0;
+        const uint16_t s1 = a1.row >= 0 ? (a1.which ? scales_up : scales)[(size_t)a1.row * G + grp] : 0;
         *reinterpret_cast<uint32_t *>(u + scale_off(codec) + w * 32 + g * 4) = (uint32_t)s0 | ((uint32_t)s1 << 16);
     }
 }
@@ -58,7 +80,18 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
                         cudaStream_t stream) {
     const int NB = (N + BLOCK_ROWS - 1) / BLOCK_ROWS;
     const int G = K / GROUP;
-    pack_kernel<<<NB * G, 256, 0, stream>>>(codec, N, K, static_cast<const uint8_t *>(canon), scales,
+    pack_kernel<<<NB * G, 256, 0, stream>>>(codec, N, K, static_cast<const uint8_t *>(canon), scales, nullptr,
+                                            nullptr, 0, static_cast<uint8_t *>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_pair(int codec, int F, int K, const void *gate, const uint16_t *gate_scales,
+                             const void *up, const uint16_t *up_scales, void *out, cudaStream_t stream) {
+    const int N = pair_rows(F);
+    const int NB = (N + BLOCK_ROWS - 1) / BLOCK_ROWS;
+    const int G = K / GROUP;
+    pack_kernel<<<NB * G, 256, 0, stream>>>(codec, N, K, static_cast<const uint8_t *>(gate), gate_scales,
+                                            static_cast<const uint8_t *>(up), up_scales, F,
                                             static_cast<uint8_t *>(out));
     return cudaGetLastError();
 }

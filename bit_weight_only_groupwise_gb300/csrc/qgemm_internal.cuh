@@ -66,11 +66,17 @@ constexpr uint32_t SUSPEND_HINT_NS = 20000;    // at most ~1.3 s per wait in tot
 
 constexpr int MAX_PARENTS = 4;
 
+// Fused outputs (qgemm_epilogue): what the kernels do where they write Y.
+enum : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2 };
+
 struct SkinnyParent {
     const uint8_t *packed;   // units of this parent
-    float *Y;                // [T][N]
-    int N, codec;
+    void *Y;                 // [T][ncols], fp32 or bf16
+    const float *R;          // EPI_ADD: residual [T][ncols]
+    int N, codec;            // N: packed rows
     int cta_begin;           // first CTA of this parent in the grid
+    int ncols;               // columns of Y: N, or F of a SwiGLU pair (N = pair_rows(F))
+    int epi, ybf16;
 };
 
 // The grid has one CTA per 16-row tile of every parent (ceil(N/16) each).
@@ -85,11 +91,36 @@ struct SkinnyArgs {
 // The wide route covers ceil(N/128) x ceil(T/128) output tiles per parent.
 struct WideParent {
     const uint8_t *packed;   // units of this parent
-    float *Y;                // [T][N]
-    int N, codec;
+    void *Y;                 // [T][ncols], fp32 or bf16
+    const float *R;          // EPI_ADD: residual [T][ncols]
+    int N, codec;            // N: packed rows
     int cta_begin;           // first output tile of this parent in its launch
     int nblocks;             // 128-row blocks
+    int ncols, epi, ybf16;   // as in SkinnyParent
 };
+
+// Where a kernel has the fp32 value v of Y[t][col] (its row `col` of the
+// packed matrix for STORE and ADD): apply the residual and store it in the
+// output type.  SwiGLU outputs go through swiglu_out with their gate and up
+// values.
+__device__ __forceinline__ void store_y(void *Y, int ybf16, size_t idx, float v) {
+    if (ybf16) reinterpret_cast<__nv_bfloat16 *>(Y)[idx] = __float2bfloat16_rn(v);
+    else reinterpret_cast<float *>(Y)[idx] = v;
+}
+
+template <class P>
+__device__ __forceinline__ void epi_out(const P &p, int t, int col, float v) {
+    const size_t idx = (size_t)t * p.ncols + col;
+    if (p.epi == EPI_ADD) v = p.R[idx] + v;
+    store_y(p.Y, p.ybf16, idx, v);
+}
+
+// silu(g) * u = g / (1 + e^-g) * u, in fp32.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// SwiGLU pair layout: packed row 16 b + i holds gate row 8 b + i (i < 8) and
+// packed row 16 b + 8 + i the up row 8 b + i.
+__host__ __device__ constexpr int pair_rows(int F) { return 16 * ((F + 7) / 8); }
 
 // ---------------------------------------------------------------- PTX wrappers
 

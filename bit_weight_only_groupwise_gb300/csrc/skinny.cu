@@ -43,6 +43,39 @@ namespace qg {
 constexpr int RING = 8;                 // groups in flight per warp
 constexpr int STAGE = 672;              // codes 512 B | int5 high words 128 B | scales 32 B
 
+// Row r, token t of a tile: the warps' partials summed in warp order.
+template <int RS>
+__device__ __forceinline__ float red_sum(const float *red, int T8, int KW, int t, int r) {
+    float v = red[t * RS + r];
+#pragma unroll 4
+    for (int q = 1; q < KW; ++q) v += red[(q * T8 + t) * RS + r];
+    return v;
+}
+
+// Write a tile's outputs through the parent's epilogue: its 16 rows (STORE,
+// ADD), or its 8 SwiGLU outputs from the gate rows 0..7 and up rows 8..15.
+template <int RS>
+__device__ __forceinline__ void write_tile(const SkinnyParent &P, const float *red, int T8, int KW, int tile,
+                                           int T) {
+    if (P.epi == EPI_SWIGLU) {
+        for (int e = threadIdx.x; e < T * 8; e += KW * 32) {
+            const int t = e >> 3, r = e & 7;
+            const int f = tile * 8 + r;
+            if (f < P.ncols)
+                store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f,
+                        silu_mul(red_sum<RS>(red, T8, KW, t, r), red_sum<RS>(red, T8, KW, t, r + 8)));
+        }
+    } else {
+        const int n0 = tile * 16;
+        const int rows = min(16, P.N - n0);
+        for (int e = threadIdx.x; e < T * 16; e += KW * 32) {
+            const int t = e >> 4, r = e & 15;
+            const float v = red_sum<RS>(red, T8, KW, t, r);
+            if (r < rows) epi_out(P, t, n0 + r, v);
+        }
+    }
+}
+
 template <int NT, int KW>
 struct SkinnySmem {
     static constexpr int RED_STRIDE = 17;                        // floats per token row (bank spread)
@@ -226,15 +259,7 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
         rw[(t + 1) * RS + g + 8] = acc[nt][3];
     }
     __syncthreads();
-    const int n0 = tile * 16;
-    const int rows = min(16, P.N - n0);
-    for (int e = threadIdx.x; e < T * 16; e += KW * 32) {
-        const int t = e >> 4, r = e & 15;
-        float v = red[t * RS + r];
-#pragma unroll
-        for (int q = 1; q < KW; ++q) v += red[(q * T8 + t) * RS + r];
-        if (r < rows) P.Y[(size_t)t * P.N + n0 + r] = v;
-    }
+    write_tile<RS>(P, red, T8, KW, tile, T);
 }
 
 // ---------------------------------------------------------------- straight-line kernels
@@ -421,14 +446,7 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
         rw[(t + 1) * RS + g + 8] = acc[nt][3];
     }
     __syncthreads();
-    const int n0 = tile * 16;
-    const int rows = min(16, P.N - n0);
-    for (int e = threadIdx.x; e < T * 16; e += KW * 32) {
-        const int t = e >> 4, r = e & 15;
-        float v = red[t * RS + r];
-        for (int q = 1; q < KW; ++q) v += red[(q * T8 + t) * RS + r];
-        if (r < rows) P.Y[(size_t)t * P.N + n0 + r] = v;
-    }
+    write_tile<RS>(P, red, T8, KW, tile, T);
 }
 
 template <int NT, int NJ, int RG>

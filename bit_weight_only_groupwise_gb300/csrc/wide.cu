@@ -439,16 +439,28 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             // ---- write this tile's Y[t][n] (consecutive lanes = consecutive rows
             // n) while the MMAs of the next tile run
             const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
+            const WideParent &P = *tr.P;
             const int n = tr.blk * BM + r;
-            if (n < tr.P->N) {
-                float *Y = tr.P->Y;
-                const int N = tr.P->N;
-                const int t0 = tr.tt * BN + hc * 64;
+            const int t0 = tr.tt * BN + hc * 64;
+            if (P.epi == EPI_SWIGLU) {
+                // lanes l and l + 8 hold the gate and the up row of one output
+                const int f = (n >> 4) * 8 + (n & 7);
+                const bool gate = (n & 8) == 0 && f < P.ncols;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float ux = __shfl_down_sync(0xffffffffu, acc[j].x, 8);
+                    const float uy = __shfl_down_sync(0xffffffffu, acc[j].y, 8);
+                    const int t = t0 + 2 * j;
+                    if (gate && t < T) store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f, silu_mul(acc[j].x, ux));
+                    if (gate && t + 1 < T)
+                        store_y(P.Y, P.ybf16, (size_t)(t + 1) * P.ncols + f, silu_mul(acc[j].y, uy));
+                }
+            } else if (n < P.N) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = t0 + 2 * j;
-                    if (t < T) Y[(size_t)t * N + n] = acc[j].x;
-                    if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[j].y;
+                    if (t < T) epi_out(P, t, n, acc[j].x);
+                    if (t + 1 < T) epi_out(P, t + 1, n, acc[j].y);
                 }
             }
         }

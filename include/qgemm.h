@@ -123,7 +123,8 @@ qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev,
 /*
  * Y[T][N] = X[T][K] . deq(W)^T on `stream`.  X (bf16 bit patterns) and Y
  * must be 16-byte aligned.  T == 0 is a no-op; T > T_max returns
- * QGEMM_ERR_T_OUT_OF_DOMAIN.
+ * QGEMM_ERR_T_OUT_OF_DOMAIN.  The plan must have the default output (STORE,
+ * F32; see qgemm_plan_set_epilogue), else QGEMM_ERR_INVALID_ARG.
  */
 qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_stream_t stream);
 
@@ -134,13 +135,74 @@ qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_
  * activation share its preparation).  All plans must have the same K and
  * T <= each plan's T_max; codecs may differ (on the tensor-core route, used
  * from T = 33 up, parents of different codecs take one launch per codec).
- * Ys[i] receives parent i's [T][N_i] result.  1 <= n_parents <= 4.
+ * Ys[i] receives parent i's [T][N_i] result.  1 <= n_parents <= 4.  Every
+ * plan must have the default output (STORE, F32).
  */
 qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
                              float *const *Ys, qgemm_stream_t stream);
 
 /* Release a plan (NULL is accepted). */
 qgemm_status qgemm_plan_destroy(qgemm_plan_t plan);
+
+/*
+ * ---------------------------------------------------------------- fused outputs
+ *
+ * The pages' projections end in two fused outputs ("ninfer-3080
+ * docs/performance.md"): a residual add on the attention o_proj and the GDN
+ * out_proj (LinearAdd, A8 prefill routes section) and the SwiGLU of the MLP's
+ * gate/up pair (route boundaries section).  A plan may carry one of them and
+ * an output type; the epilogue runs where the kernel writes Y, on the fp32
+ * result, so the GEMM's accuracy contract is unchanged:
+ *   ADD     Y[t][n] = R[t][n] + (X . deq(W)^T)[t][n]   (one fp32 add)
+ *   SWIGLU  Y[t][f] = silu(g) * u,  silu(z) = z / (1 + exp(-z)) in fp32, with
+ *           g and u row f of the gate and of the up matrix applied to X[t]
+ *   bf16    the fp32 value rounded to nearest even
+ */
+typedef enum {
+    QGEMM_EPILOGUE_STORE = 0,   /* Y = X . deq(W)^T (the default) */
+    QGEMM_EPILOGUE_ADD = 1,     /* Y = R + X . deq(W)^T, R fp32 [T][N] */
+    QGEMM_EPILOGUE_SWIGLU = 2   /* weights from qgemm_pack_pair; Y [T][F] */
+} qgemm_epilogue;
+
+typedef enum { QGEMM_OUT_F32 = 0, QGEMM_OUT_BF16 = 1 } qgemm_out;
+
+/*
+ * Bytes of the packed buffer of a SwiGLU pair of F x K matrices, or 0 for an
+ * invalid shape (as qgemm_packed_bytes; F >= 1).
+ */
+size_t qgemm_pair_packed_bytes(int F, int K, qgemm_codec codec);
+
+/*
+ * Pack the gate and the up matrix of a SwiGLU pair (each F x K, canonical codes
+ * and fp16 scales as for qgemm_pack_weights, same codec) into one buffer of
+ * qgemm_pair_packed_bytes(F, K, codec) bytes whose 16-row tiles hold 8 gate
+ * rows followed by the same 8 up rows, so that one kernel lane owns each pair.
+ * One launch plus the ordering kernel, like qgemm_pack_weights.
+ */
+qgemm_status qgemm_pack_pair(qgemm_codec codec, int F, int K,
+                             const void *gate_codes_dev, const uint16_t *gate_scales_dev,
+                             const void *up_codes_dev, const uint16_t *up_scales_dev,
+                             void *packed_dev, qgemm_stream_t stream);
+
+/*
+ * Give a plan a fused output, before qgemm_plan_bind.  For SWIGLU the plan's N
+ * is F (the output width) and the weights must come from qgemm_pack_pair.
+ * The fused outputs run through qgemm_run_ex on one matrix (qgemm_run and
+ * qgemm_run_multi take plain STORE / F32 plans only).  Returns
+ * QGEMM_ERR_INVALID_ARG for an unknown epilogue or output type, or a bound plan.
+ */
+qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue, qgemm_out out);
+
+/*
+ * Y = epilogue(X . deq(W)^T) on `stream`, for any plan.
+ *   R  ADD: fp32 [T][N], 16-byte aligned; it may be Y itself (an in-place
+ *      residual add) but must not otherwise overlap Y.  Other epilogues: NULL.
+ *   Y  [T][N] (STORE, ADD) or [T][F] (SWIGLU), fp32 or bf16 bit patterns as
+ *      the plan's output type says, 16-byte aligned.
+ * Errors as qgemm_run; a missing or superfluous R is QGEMM_ERR_INVALID_ARG.
+ */
+qgemm_status qgemm_run_ex(qgemm_plan_t plan, const void *X, int T, const void *R, void *Y,
+                          qgemm_stream_t stream);
 
 /*
  * Programmatic dependent launch (enabled by default): a run's kernel may be

@@ -49,6 +49,8 @@ WORKLOADS = {
     "prefill_a": ("prefill_a", [256, 1024, 4096]),
     "prefill_b": ("prefill_b", [256, 1024, 4096]),
     "tiny": ("tiny", [1]),
+    "linear_add": ("linear_add", [1, 2, 4, 8]),
+    "swiglu": ("swiglu", [1, 2, 4, 8]),
 }
 
 
@@ -56,7 +58,7 @@ def describe(name: str) -> dict:
     cfg = synth.CONFIGS[WORKLOADS[name][0]]
     parents = [{"N": N, "K": cfg["K"], "codec": f"int{b}"} for N, b in cfg["parents"]]
     return {"name": name, "K": cfg["K"], "parents": parents, "T": WORKLOADS[name][1],
-            "outliers": cfg["outliers"]}
+            "outliers": cfg["outliers"], "epilogue": cfg.get("epilogue", "store")}
 
 
 def weight_bytes(N: int, K: int, bits: int) -> int:
@@ -273,18 +275,32 @@ def run_ours(args, desc):
     # weights: each parent packed once, then copied so that the rotation exceeds 3x L2
     wl = synth.workload(WORKLOADS[desc["name"]][0], T_max, seed=0)
     parents = wl["parents"]
-    set_bytes = sum(qg.qgemm_packed_bytes(p["N"], K, p["bits"]) for p in parents)
+    epi = desc["epilogue"]
+    epi_code = {"store": qg.QGEMM_EPILOGUE_STORE, "add": qg.QGEMM_EPILOGUE_ADD,
+                "swiglu": qg.QGEMM_EPILOGUE_SWIGLU}[epi]
+    if epi == "swiglu":
+        # the gate/up pair (parents 0 and 1) packed as one matrix with one output
+        g, u = parents
+        base = [qg.SwiGLUPair(g["bits"], g["N"], K, g["packed"], g["scales"], u["packed"], u["scales"], T_max)]
+        set_bytes = qg.qgemm_pair_packed_bytes(g["N"], K, g["bits"])
+        out_cols = [g["N"]]
+    else:
+        base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max, epilogue=epi_code)
+                for p in parents]
+        set_bytes = sum(qg.qgemm_packed_bytes(p["N"], K, p["bits"]) for p in parents)
+        out_cols = [p["N"] for p in parents]
     copies = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)))
     weight_sets = []
-    base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max) for p in parents]
     for i in range(copies):
         ws = []
         for b in base:
-            w = qg.GroupwiseWeights.__new__(qg.GroupwiseWeights)
-            w.codec, w.N, w.K, w.T_max = b.codec, b.N, b.K, b.T_max
+            w = type(b).__new__(type(b))
+            w.codec, w.N, w.K, w.T_max, w.epilogue, w.out = b.codec, b.N, b.K, b.T_max, b.epilogue, b.out
             w.packed = b.packed.clone() if i else b.packed
             st, w.plan = qg.qgemm_plan(b.N, K, b.codec, T_max)
             qg.check(st, "qgemm_plan")
+            if epi != "store":
+                qg.check(qg.qgemm_plan_set_epilogue(w.plan, epi_code, qg.QGEMM_OUT_F32), "set_epilogue")
             wsb = qg.qgemm_plan_workspace_bytes(w.plan)
             w.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
             qg.check(qg.qgemm_plan_bind(w.plan, w.packed, w.workspace, w.workspace.numel()), "bind")
@@ -292,13 +308,19 @@ def run_ours(args, desc):
             ws.append(w)
         weight_sets.append(ws)
     xs = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).to(dev) for T in Ts}
-    ys = {T: [torch.empty((T, p["N"]), dtype=torch.float32, device=dev) for p in parents] for T in Ts}
+    ys = {T: [torch.empty((T, n), dtype=torch.float32, device=dev) for n in out_cols] for T in Ts}
+    # the residual of a LinearAdd: fp32 [T, N], seeded
+    rs = {T: torch.from_numpy(np.random.default_rng(T).normal(0, 8, (T, out_cols[0])).astype(np.float32)).to(dev)
+          for T in Ts} if epi == "add" else {}
     torch.cuda.synchronize()
 
-    def call(ws, T, X=None, Ys=None):
+    def call(ws, T, X=None, Ys=None, Rt=None):
         X = xs[T] if X is None else X
         Ys = ys[T] if Ys is None else Ys
-        if len(ws) == 1:
+        if epi != "store":
+            Rt = (rs[T] if Rt is None else Rt) if epi == "add" else None
+            st = qg.qgemm_run_ex(ws[0].plan, X, T, Rt, Ys[0], torch.cuda.current_stream())
+        elif len(ws) == 1:
             st = qg.qgemm_run(ws[0].plan, X, T, Ys[0], torch.cuda.current_stream())
         else:
             st = qg.qgemm_run_multi([w.plan for w in ws], X, T, Ys, torch.cuda.current_stream())
@@ -408,9 +430,11 @@ def run_ours(args, desc):
     e2e = None
     if not args.no_e2e:
         hx = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).pin_memory() for T in Ts}
-        hy = {T: [torch.empty((T, p["N"]), dtype=torch.float32).pin_memory() for p in parents] for T in Ts}
+        hy = {T: [torch.empty((T, n), dtype=torch.float32).pin_memory() for n in out_cols] for T in Ts}
         dx = {T: torch.empty_like(xs[T]) for T in Ts}
-        h2d = sum(hx[T].numel() * 2 for T in Ts)
+        hr = {T: rs[T].cpu().pin_memory() for T in rs}
+        dr = {T: torch.empty_like(rs[T]) for T in rs}
+        h2d = sum(hx[T].numel() * 2 for T in Ts) + sum(hr[T].numel() * 4 for T in hr)
         d2h = sum(y.numel() * 4 for T in Ts for y in hy[T])
         e_steps = max(1, min(args.steps, 2000))
         barrier(world)
@@ -421,7 +445,9 @@ def run_ours(args, desc):
         for i in range(e_steps):
             for T in Ts:
                 dx[T].copy_(hx[T], non_blocking=True)
-                call(weight_sets[i % copies], T, X=dx[T])
+                if epi == "add":
+                    dr[T].copy_(hr[T], non_blocking=True)
+                call(weight_sets[i % copies], T, X=dx[T], Rt=dr.get(T))
                 for y, h in zip(ys[T], hy[T]):
                     h.copy_(y, non_blocking=True)
             stream.synchronize()          # the step's results are on the host
@@ -444,6 +470,7 @@ def run_ours(args, desc):
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": desc["name"], "parents": desc["parents"], "K": desc["K"], "T": Ts,
+                       "epilogue": epi,
                        "l2": f"rotating {copies} packed-weight copies ({copies * set_bytes / 1e6:.0f} MB > 3x L2)",
                        "parallelism": "replicas" if world > 1 else "single",
                        "pdl": not args.no_pdl},

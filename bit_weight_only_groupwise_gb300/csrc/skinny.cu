@@ -65,6 +65,15 @@ __device__ __forceinline__ void write_tile(const SkinnyParent &P, const float *r
                 store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f,
                         silu_mul(red_sum<RS>(red, T8, KW, t, r), red_sum<RS>(red, T8, KW, t, r + 8)));
         }
+    } else if (P.epi == EPI_STORE && !P.ybf16) {
+        float *Y = static_cast<float *>(P.Y);
+        const int n0 = tile * 16;
+        const int rows = min(16, P.N - n0);
+        for (int e = threadIdx.x; e < T * 16; e += KW * 32) {
+            const int t = e >> 4, r = e & 15;
+            const float v = red_sum<RS>(red, T8, KW, t, r);
+            if (r < rows) Y[(size_t)t * P.ncols + n0 + r] = v;
+        }
     } else {
         const int n0 = tile * 16;
         const int rows = min(16, P.N - n0);

@@ -201,9 +201,37 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 // ---------------------------------------------------------------- the kernel
 
+// Fused outputs of one tile's accumulators (thread = row n, tokens t0 + 2j,
+// t0 + 2j + 1): residual add, bf16, or SwiGLU, where lanes l and l + 8 hold
+// the gate and the up row of one output.
+__device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t0, int T, const float2 (&acc)[32]) {
+    if (P.epi == EPI_SWIGLU) {
+        const int f = (n >> 4) * 8 + (n & 7);
+        const bool gate = (n & 8) == 0 && f < P.ncols;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float ux = __shfl_down_sync(0xffffffffu, acc[j].x, 8);
+            const float uy = __shfl_down_sync(0xffffffffu, acc[j].y, 8);
+            const int t = t0 + 2 * j;
+            if (gate && t < T) store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f, silu_mul(acc[j].x, ux));
+            if (gate && t + 1 < T) store_y(P.Y, P.ybf16, (size_t)(t + 1) * P.ncols + f, silu_mul(acc[j].y, uy));
+        }
+    } else if (n < P.N) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = t0 + 2 * j;
+            if (t < T) epi_out(P, t, n, acc[j].x);
+            if (t + 1 < T) epi_out(P, t + 1, n, acc[j].y);
+        }
+    }
+}
+
 // CODEC: the codec of every parent of the launch (4 or 5); a launch whose
-// parents mix codecs is split into one launch per codec by the host.
-template <int CODEC>
+// parents mix codecs is split into one launch per codec by the host.  FUSED:
+// the launch's parent has a fused output (residual add, SwiGLU or bf16); the
+// plain instantiation keeps the store loop, and the code, of the plain GEMM
+// (the fused store code in every launch measured 12% slower at T = 4096).
+template <int CODEC, bool FUSED>
 __global__ void __launch_bounds__(wide::THREADS, 1)
     wide_kernel(const __grid_constant__ WideArgs args, const __grid_constant__ CUtensorMap xmap) {
     using namespace wide;
@@ -439,28 +467,18 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             // ---- write this tile's Y[t][n] (consecutive lanes = consecutive rows
             // n) while the MMAs of the next tile run
             const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
-            const WideParent &P = *tr.P;
             const int n = tr.blk * BM + r;
-            const int t0 = tr.tt * BN + hc * 64;
-            if (P.epi == EPI_SWIGLU) {
-                // lanes l and l + 8 hold the gate and the up row of one output
-                const int f = (n >> 4) * 8 + (n & 7);
-                const bool gate = (n & 8) == 0 && f < P.ncols;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float ux = __shfl_down_sync(0xffffffffu, acc[j].x, 8);
-                    const float uy = __shfl_down_sync(0xffffffffu, acc[j].y, 8);
-                    const int t = t0 + 2 * j;
-                    if (gate && t < T) store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f, silu_mul(acc[j].x, ux));
-                    if (gate && t + 1 < T)
-                        store_y(P.Y, P.ybf16, (size_t)(t + 1) * P.ncols + f, silu_mul(acc[j].y, uy));
-                }
-            } else if (n < P.N) {
+            if constexpr (FUSED) {
+                wide_fused_out(*tr.P, n, tr.tt * BN + hc * 64, T, acc);
+            } else if (n < tr.P->N) {
+                float *Y = static_cast<float *>(tr.P->Y);
+                const int N = tr.P->ncols;
+                const int t0 = tr.tt * BN + hc * 64;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = t0 + 2 * j;
-                    if (t < T) epi_out(P, t, n, acc[j].x);
-                    if (t + 1 < T) epi_out(P, t + 1, n, acc[j].y);
+                    if (t < T) Y[(size_t)t * N + n] = acc[j].x;
+                    if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[j].y;
                 }
             }
         }
@@ -522,7 +540,7 @@ static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K) {
 
 int wide_tile_tokens() { return wide::BN; }
 
-template <int CODEC>
+template <int CODEC, bool FUSED>
 static cudaError_t launch_codec(const WideParent *parents, int np, const CUtensorMap &xmap, int T, int K,
                                 unsigned int *status, cudaStream_t stream) {
     static bool attr_set[64] = {};
@@ -532,7 +550,8 @@ static cudaError_t launch_codec(const WideParent *parents, int np, const CUtenso
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(wide_kernel<CODEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, wide::Smem::BYTES);
+        e = cudaFuncSetAttribute(wide_kernel<CODEC, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 wide::Smem::BYTES);
         if (e != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         attr_set[dev] = true;
@@ -559,7 +578,7 @@ static cudaError_t launch_codec(const WideParent *parents, int np, const CUtenso
     // persistent: one CTA per SM (its shared memory allows no more), each
     // taking the tiles blockIdx.x, blockIdx.x + grid, ...
     const int grid = tiles < sms[dev] ? tiles : sms[dev];
-    wide_kernel<CODEC><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
+    wide_kernel<CODEC, FUSED><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
     return cudaGetLastError();
 }
 
@@ -570,9 +589,17 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
     cudaError_t e = make_xmap(&xmap, X, T, K);
     if (e != cudaSuccess) return e;
     int n4 = 0, n5 = 0;
-    for (int i = 0; i < np; ++i) (parents[i].codec == 4 ? n4 : n5)++;
-    if (n4 && (e = launch_codec<4>(parents, np, xmap, T, K, status, stream)) != cudaSuccess) return e;
-    if (n5 && (e = launch_codec<5>(parents, np, xmap, T, K, status, stream)) != cudaSuccess) return e;
+    bool fused = false;
+    for (int i = 0; i < np; ++i) {
+        (parents[i].codec == 4 ? n4 : n5)++;
+        fused = fused || parents[i].epi != EPI_STORE || parents[i].ybf16;
+    }
+    if (n4 && (e = fused ? launch_codec<4, true>(parents, np, xmap, T, K, status, stream)
+                         : launch_codec<4, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
+        return e;
+    if (n5 && (e = fused ? launch_codec<5, true>(parents, np, xmap, T, K, status, stream)
+                         : launch_codec<5, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
+        return e;
     *launches = (n4 > 0) + (n5 > 0);
     return cudaSuccess;
 }

@@ -206,6 +206,11 @@ CONFIGS = {
     "multi": dict(parents=[(4096, 4), (12288, 5)], K=5120, Ts=[4, 16, 64], outliers=True),
     "prefill_a": dict(parents=[(7168, 4)], K=5120, Ts=[256, 1024, 4096], outliers=True),
     "prefill_b": dict(parents=[(5120, 4)], K=6144, Ts=[256, 1024, 4096], outliers=True),
+    # fused outputs at decode widths: the Q5 [5120, 6144] LinearAdd of the
+    # attention o_proj / GDN out_proj, and the Q4 gate_up projection (34816 x
+    # 5120) as a SwiGLU pair of two 17408-row matrices (parents 0 and 1)
+    "linear_add": dict(parents=[(5120, 5)], K=6144, Ts=[1, 2, 4, 8], outliers=True, epilogue="add"),
+    "swiglu": dict(parents=[(17408, 4), (17408, 4)], K=5120, Ts=[1, 2, 4, 8], outliers=True, epilogue="swiglu"),
 }
 
 

@@ -122,9 +122,16 @@ def fp64_to_fp16_bits(x: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------- draws
 
 def uniform_codes(seed: int, tid: int, N: int, K: int, bits: int) -> np.ndarray:
-    """int8 codes [N, K], uniform over the b-bit two's-complement range."""
+    """int8 codes [N, K], uniform over the b-bit two's-complement range; for
+    bits = 8, uint8 E4M3 codes uniform over the 254 that are not NaN (a NaN
+    code S.1111.111 is replaced by S.1111.110, the largest finite value)."""
+    if bits == 8:
+        z = draws(seed, tid, 0, N * K)
+        u = (z >> np.uint64(56)).astype(np.uint8)
+        u[(u & 0x7F) == 0x7F] ^= np.uint8(1)
+        return u.reshape(N, K)
     if bits not in (4, 5):
-        raise ValueError("bits must be 4 or 5")
+        raise ValueError("bits must be 4, 5 or 8")
     z = draws(seed, tid, 0, N * K)
     u = (z >> np.uint64(64 - bits)).astype(np.int16)
     return (u - (1 << (bits - 1))).astype(np.int8).reshape(N, K)
@@ -160,9 +167,12 @@ def row_bytes(K: int, bits: int) -> int:
 
 
 def pack_canonical(codes: np.ndarray, bits: int) -> np.ndarray:
-    """Encode int codes [N, K] in the canonical packed format (uint8 [N, row_bytes])."""
+    """Encode codes [N, K] in the canonical packed format (uint8 [N, row_bytes]);
+    fp8 codes are their own canonical bytes."""
     codes = np.asarray(codes)
     N, K = codes.shape
+    if bits == 8:
+        return np.ascontiguousarray(codes, dtype=np.uint8).copy()
     lo = -(1 << (bits - 1))
     hi = (1 << (bits - 1)) - 1
     if codes.size and (codes.min() < lo or codes.max() > hi):

@@ -20,7 +20,11 @@
  * - an fp64 oracle as the accuracy yardstick (same page, the A8 prefill
  *   routes section, which reports relative L2 against an FP64 oracle);
  * - codes are symmetric two's complement with no zero point: int4 in [-8, 7],
- *   int5 in [-16, 15]; scales are IEEE fp16; activations are bf16.
+ *   int5 in [-16, 15]; scales are IEEE fp16; activations are bf16;
+ * - the FP8 codec (the FP8-weight kernel the "Speculative decoding" page checks
+ *   at verify widths) holds OCP E4M3 codes: sign, 4 exponent bits with bias 7,
+ *   3 mantissa bits, subnormals at exponent 0, no infinities, and NaN for the
+ *   two codes S.1111.111; with the same fp16 scale per 64 columns.
  *
  * Every product x * s * q is exact in fp64 (bf16 has 8 significant bits,
  * fp16 11, a code at most 5), so the only roundings are those of the running
@@ -29,6 +33,7 @@
  * Canonical packing read here (the library's input format):
  * - int4: ceil(K/2) bytes per row; byte j holds code 2j in bits 0-3 and code
  *   2j+1 in bits 4-7.
+ * - fp8: K bytes per row, byte k = the E4M3 code of column k.
  * - int5: ceil(5K/8) bytes per row; LSB-first bitstream, code k in bits
  *   5k .. 5k+4.
  * Scales: fp16 bit patterns, row-major [N][ceil(K/64)]; the last group of a
@@ -81,9 +86,25 @@ static double oracle_bf16_to_double(uint16_t b)
 
 int qgemm_oracle_row_bytes(int bits, int K)
 {
-    if ((bits != 4 && bits != 5) || K < 0)
+    if ((bits != 4 && bits != 5 && bits != 8) || K < 0)
         return -1;
     return (int)(((long)K * bits + 7) / 8);
+}
+
+/* OCP FP8 E4M3 -> double, from the field definitions. */
+static double oracle_e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7;
+    int expo = (b >> 3) & 0x0f;
+    int mant = b & 0x07;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant, -9);                  /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp((double)(8 + mant), expo - 10);     /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
 }
 
 int qgemm_oracle_groups(int K)
@@ -109,7 +130,15 @@ static int oracle_code(int bits, const uint8_t *row, int k)
     }
 }
 
-/* Integer codes [N][K] (unpacking only). */
+/* Value of code k of one canonical row: the integer code, or the E4M3 value. */
+static double oracle_value(int bits, const uint8_t *row, int k)
+{
+    if (bits == 8)
+        return oracle_e4m3_to_double(row[k]);
+    return (double)oracle_code(bits, row, k);
+}
+
+/* Integer codes [N][K] (unpacking only; fp8 codes come back as their bytes). */
 int qgemm_oracle_unpack(int bits, int N, int K, const uint8_t *packed, int8_t *codes)
 {
     int rb = qgemm_oracle_row_bytes(bits, K);
@@ -117,7 +146,8 @@ int qgemm_oracle_unpack(int bits, int N, int K, const uint8_t *packed, int8_t *c
         return -1;
     for (int n = 0; n < N; ++n)
         for (int k = 0; k < K; ++k)
-            codes[(size_t)n * K + k] = (int8_t)oracle_code(bits, packed + (size_t)n * rb, k);
+            codes[(size_t)n * K + k] = bits == 8 ? (int8_t)packed[(size_t)n * rb + k]
+                                                 : (int8_t)oracle_code(bits, packed + (size_t)n * rb, k);
     return 0;
 }
 
@@ -133,7 +163,7 @@ int qgemm_oracle_dequant(int bits, int N, int K, const uint8_t *packed,
         const uint8_t *row = packed + (size_t)n * rb;
         for (int k = 0; k < K; ++k) {
             double s = oracle_half_to_double(scales[(size_t)n * G + k / ORACLE_GROUP]);
-            W[(size_t)n * K + k] = s * (double)oracle_code(bits, row, k);
+            W[(size_t)n * K + k] = s * oracle_value(bits, row, k);
         }
     }
     return 0;
@@ -160,7 +190,7 @@ int qgemm_oracle_gemm(int bits, int N, int K, int T, const uint8_t *packed,
         const uint8_t *row = packed + (size_t)n * rb;
         for (int k = 0; k < K; ++k) {
             double s = oracle_half_to_double(scales[(size_t)n * G + k / ORACLE_GROUP]);
-            w[k] = s * (double)oracle_code(bits, row, k);
+            w[k] = s * oracle_value(bits, row, k);
         }
         for (int t = 0; t < T; ++t) {
             const uint16_t *xr = X + (size_t)t * K;

@@ -269,9 +269,45 @@ def rng_free_dot(x_bits, codes):
     return xv @ codes.astype(np.int64).T
 
 
+def fp8_values_torch(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes -> fp64 through torch's float8_e4m3fn type (a library routine)."""
+    torch = pytest.importorskip("torch")
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_fp8_decode(lib):
+    # every byte once, unit scales: the dequantised row is the codes' values
+    codes = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    ones = np.full((1, 4), 0x3C00, np.uint16)
+    W = oracle.dequant(8, codes, ones, 1, 256, lib=lib)[0]
+    ref = fp8_values_torch(codes[0])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(W), nan) and nan.sum() == 2
+    assert np.array_equal(W[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(W[~nan]), np.signbit(ref[~nan]))      # -0.0 included
+    # closed forms: 1.0, the largest value, the smallest subnormal and normal
+    assert (W[0x38], W[0x7E], W[0x01], W[0x08], W[0xB8]) == (1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -1.0)
+
+
+def pin_fp8_gemm(lib):
+    N, K, T = 11, 192, 3
+    codes = synth.uniform_codes(51, 1, N, K, 8)
+    scales = synth.group_scales(51, 2, N, K)
+    x = synth.activations(51, T, K, outliers=True)
+    Y, A = oracle.gemm(8, codes, scales, x, N, K, lib=lib)
+    w = fp8_values_torch(codes) * np.repeat(fp16_values(scales), 64, axis=1)[:, :K]
+    xv = bf16_values(x)
+    ref = xv @ w.T
+    mag = np.abs(xv) @ np.abs(w).T
+    assert np.all(np.abs(Y - ref) <= 2 * K * U * mag)
+    assert np.allclose(A, mag, rtol=4 * K * U)
+
+
 PINS = [pin_golden, pin_exact_rational, pin_bruteforce_int4, pin_bruteforce_int5, pin_numpy_matmul,
         pin_linearity_exact, pin_identity_and_permutation, pin_scaling_and_negation,
-        pin_int5_contains_int4, pin_column_independence, pin_swiglu, pin_linear_add]
+        pin_int5_contains_int4, pin_column_independence, pin_swiglu, pin_linear_add, pin_fp8_decode,
+        pin_fp8_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -286,9 +322,9 @@ MUTANTS = {
                           "for (int k = 0; k < K - 1; ++k) {\n                double p"),
     "sign_extension": ("return nib >= 8 ? nib - 16 : nib;", "return nib > 8 ? nib - 16 : nib;"),
     "nibble_order": ("(k & 1) ? (byte >> 4) : (byte & 0x0f)", "(k & 1) ? (byte & 0x0f) : (byte >> 4)"),
-    "transposed_scales": ("w[k] = s * (double)oracle_code(bits, row, k);",
+    "transposed_scales": ("w[k] = s * oracle_value(bits, row, k);",
                           "w[k] = oracle_half_to_double(scales[(size_t)(k / ORACLE_GROUP) * N + n])"
-                          " * (double)oracle_code(bits, row, k); (void)s;"),
+                          " * oracle_value(bits, row, k); (void)s;"),
     "int5_sign": ("return v >= 16 ? v - 32 : v;", "return v >= 16 ? v - 31 : v;"),
     "int5_bit_order": ("& 1) << b;", "& 1) << (4 - b);"),
     "abs_sum": ("mag += fabs(p);", "mag += p;"),
@@ -301,6 +337,10 @@ MUTANTS = {
                              "out[i] = u[i] / (1.0 + exp(-u[i])) * g[i];"),
     "residual_dropped": ("Y[i] = (double)R[i] + Y[i];", "Y[i] = Y[i];"),
     "residual_abs": ("A[i] = fabs((double)R[i]) + A[i];", "A[i] = (double)R[i] + A[i];"),
+    "e4m3_bias": ("ldexp((double)(8 + mant), expo - 10);", "ldexp((double)(8 + mant), expo - 9);"),
+    "e4m3_subnormal": ("ldexp((double)mant, -9);", "ldexp((double)mant, -10);"),
+    "e4m3_nan": ("if (expo == 15 && mant == 7)", "if (expo == 15)"),
+    "e4m3_sign": ("int sign = b >> 7;", "int sign = (b >> 6) & 1;"),
 }
 
 

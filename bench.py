@@ -51,14 +51,19 @@ WORKLOADS = {
     "tiny": ("tiny", [1]),
     "linear_add": ("linear_add", [1, 2, 4, 8]),
     "swiglu": ("swiglu", [1, 2, 4, 8]),
+    "decode_fp8": ("decode_fp8", [1, 2, 4, 8]),
 }
 
 
 def describe(name: str) -> dict:
     cfg = synth.CONFIGS[WORKLOADS[name][0]]
-    parents = [{"N": N, "K": cfg["K"], "codec": f"int{b}"} for N, b in cfg["parents"]]
+    parents = [{"N": N, "K": cfg["K"], "codec": "fp8" if b == 8 else f"int{b}"} for N, b in cfg["parents"]]
     return {"name": name, "K": cfg["K"], "parents": parents, "T": WORKLOADS[name][1],
             "outliers": cfg["outliers"], "epilogue": cfg.get("epilogue", "store")}
+
+
+def codec_bits(codec: str) -> int:
+    return 8 if codec == "fp8" else int(codec[3:])
 
 
 def weight_bytes(N: int, K: int, bits: int) -> int:
@@ -70,7 +75,7 @@ def step_bytes(desc) -> int:
     K = desc["K"]
     total = 0
     for T in desc["T"]:
-        total += sum(weight_bytes(p["N"], K, int(p["codec"][3:])) for p in desc["parents"]) + 2 * T * K
+        total += sum(weight_bytes(p["N"], K, codec_bits(p["codec"])) for p in desc["parents"]) + 2 * T * K
     return total
 
 
@@ -394,7 +399,7 @@ def run_ours(args, desc):
     per_T = {}
     by_kernel = {}          # kernel -> [time ms, bytes, flops, launches] over the timed region
     for T in Ts:
-        b = sum(weight_bytes(p["N"], K, int(p["codec"][3:])) for p in desc["parents"]) + 2 * T * K
+        b = sum(weight_bytes(p["N"], K, codec_bits(p["codec"])) for p in desc["parents"]) + 2 * T * K
         flops = sum(2 * T * p["N"] * K for p in desc["parents"])
         med = statistics.median(per_T_ms[T])
         mean = statistics.fmean(per_T_ms[T])

@@ -32,6 +32,7 @@ QGEMM_ERR_UNSUPPORTED = 8
 
 QGEMM_INT4 = 4
 QGEMM_INT5 = 5
+QGEMM_FP8 = 8
 
 QGEMM_EPILOGUE_STORE = 0
 QGEMM_EPILOGUE_ADD = 1

@@ -15,9 +15,10 @@ cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16
 cudaError_t launch_fence(cudaStream_t stream);
 cudaError_t launch_pack_pair(int codec, int F, int K, const void *gate, const uint16_t *gate_scales,
                              const void *up, const uint16_t *up_scales, void *out, cudaStream_t stream);
-cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, bool f8, cudaStream_t stream);
 int skinny_line_groups(int G, int nj_pref);
-cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream);
+cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, bool f8,
+                               cudaStream_t stream);
 cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
                         cudaStream_t stream, int *launches);
 }  // namespace qg
@@ -106,7 +107,10 @@ static unsigned int *status_ptr() {
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5; }
+static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5 || c == QGEMM_FP8; }
+
+// FP8 weights are served on the small-T routes only (token tiles up to 32).
+constexpr int FP8_T_MAX = 32;
 
 extern "C" {
 
@@ -153,6 +157,7 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     *out = nullptr;
     if (!valid_codec(codec) || T_max < 1) return QGEMM_ERR_INVALID_ARG;
     if (N < 1 || K < GROUP || K % GROUP) return QGEMM_ERR_SHAPE;
+    if (codec == QGEMM_FP8 && T_max > FP8_T_MAX) return QGEMM_ERR_T_OUT_OF_DOMAIN;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
@@ -300,6 +305,8 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     unsigned int *status = status_ptr();
     if (!status) return QGEMM_ERR_CUDA;
     if (route == ROUTE_WIDE128) {
+        for (int i = 0; i < np; ++i)
+            if (plans[i]->codec == QGEMM_FP8) return QGEMM_ERR_T_OUT_OF_DOMAIN;   // small-T routes only
         WideParent wp[MAX_PARENTS];
         memset(wp, 0, sizeof wp);
         for (int i = 0; i < np; ++i) {
@@ -332,9 +339,11 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     a.T = T;
     a.K = K;
     a.G = G;
+    bool f8 = false;
+    for (int i = 0; i < np; ++i) f8 = f8 || plans[i]->codec == QGEMM_FP8;
     const int nj = skinny_line_groups(G, line);
-    const cudaError_t e = nj ? launch_skinny_line(a, route_tokens(route) / 8, nj, grid, pdl, stream)
-                             : launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, stream);
+    const cudaError_t e = nj ? launch_skinny_line(a, route_tokens(route) / 8, nj, grid, pdl, f8, stream)
+                             : launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, f8, stream);
     if (e != cudaSuccess) return QGEMM_ERR_CUDA;
     g_launches.fetch_add(1);
     return QGEMM_OK;

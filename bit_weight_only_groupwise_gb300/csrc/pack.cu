@@ -35,6 +35,25 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
     const int UB = unit_bytes(codec);
     uint8_t *u = out + (size_t)unit * UB;
 
+    if (codec == 8) {
+        // E4M3 codes: the lane's 32-byte chunk, row r0 then row r1, each word
+        // holding k = 4j .. 4j+3 in byte order (4j, 4j+2, 4j+1, 4j+3)
+        uint32_t w8[8];
+        for (int half = 0; half < 2; ++half) {
+            const SrcRow sr = src_row(b * BLOCK_ROWS + 16 * w + g + 8 * half, N, F);
+            const uint8_t *src = (sr.which ? canon_up : canon) + (size_t)(sr.row < 0 ? 0 : sr.row) * K +
+                                 grp * GROUP + 16 * c;
+            for (int j = 0; j < 4; ++j) {
+                uint32_t v = 0;
+                if (sr.row >= 0)
+                    v = (uint32_t)src[4 * j] | ((uint32_t)src[4 * j + 2] << 8) | ((uint32_t)src[4 * j + 1] << 16) |
+                        ((uint32_t)src[4 * j + 3] << 24);
+                w8[4 * half + j] = v;
+            }
+        }
+        *reinterpret_cast<uint4 *>(u + w * 1024 + lane * 32) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+        *reinterpret_cast<uint4 *>(u + w * 1024 + lane * 32 + 16) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+    } else {
     uint32_t words[4] = {0, 0, 0, 0};
     uint32_t hi = 0;
     for (int half = 0; half < 2; ++half) {          // rows r0 and r0 + 8
@@ -67,6 +86,7 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
     }
     *reinterpret_cast<uint4 *>(u + w * 512 + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
     if (codec == 5) *reinterpret_cast<uint32_t *>(u + NIB_BYTES + w * 128 + lane * 4) = hi;
+    }
     if (c == 0) {
         const SrcRow a0 = src_row(b * BLOCK_ROWS + 16 * w + g, N, F);
         const SrcRow a1 = src_row(b * BLOCK_ROWS + 16 * w + g + 8, N, F);

@@ -23,6 +23,13 @@
 // Scale pair i of tile w is (s[16w + i], s[16w + i + 8]).
 // Rows n >= N (padding of the last block) hold u = bias (q = 0) and s = 0.
 //
+// FP8 (E4M3) units: the lane's chunk is 32 bytes, row r0's 16 codes (k 16c ..
+// 16c+15) in words 0..3 and row r1's in words 4..7; word j of a row holds k
+// = 4j .. 4j+3 in byte order (4j, 4j+2, 4j+1, 4j+3), so that the k pair
+// (4j, 4j+1) sits in bytes 0 and 2 and (4j+2, 4j+3) in bytes 1 and 3.  The
+// code plane (8 tiles x 1024 B) is followed by the scales as above.  Padding
+// rows hold code 0 (+0.0) and s = 0.
+//
 // Decode: OR a biased code into the mantissa of bf16 128.0 (0x4300; the
 // mantissa of [128, 256) counts in steps of 1) and subtract 128 + bias: the
 // result is the exact integer q as bf16, with no integer-to-float conversion.
@@ -45,9 +52,15 @@ constexpr int HI_BYTES = 1024;             // int5 high-bit plane of a unit
 constexpr int SCALE_BYTES = 256;           // 128 fp16 scales
 constexpr int UNIT4 = NIB_BYTES + SCALE_BYTES;
 constexpr int UNIT5 = NIB_BYTES + HI_BYTES + SCALE_BYTES;
+constexpr int CODE8_BYTES = 8192;          // fp8 code plane of a unit: 8 tiles x 32 lanes x 32 B
+constexpr int UNIT8 = CODE8_BYTES + SCALE_BYTES;
 
-__host__ __device__ constexpr int unit_bytes(int codec) { return codec == 5 ? UNIT5 : UNIT4; }
-__host__ __device__ constexpr int scale_off(int codec) { return codec == 5 ? NIB_BYTES + HI_BYTES : NIB_BYTES; }
+__host__ __device__ constexpr int unit_bytes(int codec) {
+    return codec == 8 ? UNIT8 : codec == 5 ? UNIT5 : UNIT4;
+}
+__host__ __device__ constexpr int scale_off(int codec) {
+    return codec == 8 ? CODE8_BYTES : codec == 5 ? NIB_BYTES + HI_BYTES : NIB_BYTES;
+}
 
 // nibble position of k offset j (0..7) inside a code word
 __host__ __device__ constexpr int nib_pos(int j) { return (j >> 1) + 4 * (j & 1); }
@@ -284,6 +297,25 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 template <int SHIFT>
 __device__ __forceinline__ uint32_t dec4_pair(uint32_t w) {
     return bf16x2_sub(and_or(w >> SHIFT, 0x000F000Fu, 0x43004300u), 0x43084308u);   // - (128 + 8)
+}
+
+// FP8: two E4M3 codes as an exact bf16x2 pair.  An E4M3 code's 7 magnitude
+// bits placed at bf16 bits 4..10 (exponent field = the code's exponent,
+// mantissa = its 3 bits) read as the code's value times 2^-120, subnormal
+// codes included; the sign goes to bit 15, and one bf16x2 multiply by 2^120
+// (exact: a power of two, results in the normal range) gives the value.
+// Codes in bytes 0 and 2 of w (SHI = 0) or in bytes 1 and 3 (SHI = 1).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+template <int SHI>
+__device__ __forceinline__ uint32_t dec8_pair(uint32_t w) {
+    const uint32_t mag = (SHI ? (w >> 4) : (w << 4)) & 0x07F007F0u;
+    const uint32_t sgn = SHI ? w : (w << 8);
+    return bf16x2_mul(and_or(sgn, 0x80008000u, mag), 0x7B807B80u);   // x 2^120
 }
 
 // int5: nibble pair plus the two high bits taken from the lane's high word.

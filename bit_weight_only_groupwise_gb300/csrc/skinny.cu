@@ -42,6 +42,8 @@ namespace qg {
 
 constexpr int RING = 8;                 // groups in flight per warp
 constexpr int STAGE = 672;              // codes 512 B | int5 high words 128 B | scales 32 B
+constexpr int STAGE8 = 1056;            // fp8: codes 1024 B | scales 32 B
+constexpr int SC8 = 1024;               // fp8: offset of the scale pairs in a stage
 
 // Row r, token t of a tile: the warps' partials summed in warp order.
 template <int RS>
@@ -85,10 +87,10 @@ __device__ __forceinline__ void write_tile(const SkinnyParent &P, const float *r
     }
 }
 
-template <int NT, int KW>
+template <int NT, int KW, int ST = STAGE>
 struct SkinnySmem {
     static constexpr int RED_STRIDE = 17;                        // floats per token row (bank spread)
-    static constexpr int RINGS = KW * RING * STAGE;
+    static constexpr int RINGS = KW * RING * ST;
     static constexpr int RED = KW * NT * 8 * RED_STRIDE * 4;     // [KW][8*NT][16] partials
     static constexpr int BYTES = RINGS + RED;
 };
@@ -114,6 +116,19 @@ __device__ __forceinline__ void decode_tile(int codec, uint4 cw, uint32_t hw, ui
     }
 }
 
+// FP8 A fragments from the lane's 32-byte chunk: lo = row g, hi = row g+8,
+// word q of a row = k 4q .. 4q+3 (pairs in bytes 0/2 and 1/3).
+__device__ __forceinline__ void decode_tile8(uint4 lo, uint4 hi, uint32_t (&a)[4][4]) {
+    const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        a[q][0] = dec8_pair<0>(l[q]);
+        a[q][1] = dec8_pair<0>(h[q]);
+        a[q][2] = dec8_pair<1>(l[q]);
+        a[q][3] = dec8_pair<1>(h[q]);
+    }
+}
+
 // One CTA per 16-row tile: KW warps split the tile's K groups (warp kw takes
 // groups kw, kw + KW, ...), each streaming its groups through a private ring
 // of RING stages; then the CTA sums the warps' partials in warp order.
@@ -121,10 +136,11 @@ __device__ __forceinline__ void decode_tile(int codec, uint4 cw, uint32_t hw, ui
 // The loop is unrolled by the ring depth so that stage offsets are immediates,
 // and every global address advances by a constant stride: the integer pipe,
 // which also carries the nibble unpacking, is the tightest resource here.
-template <int NT, int KW>
+// ST: the stage size, STAGE8 when a parent of the launch holds FP8 codes.
+template <int NT, int KW, int ST>
 __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__ SkinnyArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int RS = SkinnySmem<NT, KW>::RED_STRIDE;
+    constexpr int RS = SkinnySmem<NT, KW, ST>::RED_STRIDE;
     constexpr int T8 = 8 * NT;
 
     // ---- which parent and tile this CTA owns
@@ -142,19 +158,22 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
     const int kw = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int T = args.T;
-    uint8_t *ring = smem + kw * RING * STAGE;
-    float *red = reinterpret_cast<float *>(smem + SkinnySmem<NT, KW>::RINGS);
+    uint8_t *ring = smem + kw * RING * ST;
+    float *red = reinterpret_cast<float *>(smem + SkinnySmem<NT, KW, ST>::RINGS);
     const int nj = (G - kw + KW - 1) / KW;           // groups of this warp: kw + KW*j
 
-    // per-lane copy plan: every lane its 16-byte code chunk; lanes 8..15 the
-    // int5 high words; lanes 16..17 the scale pairs
-    const uint8_t *src = P.packed + ((size_t)b * G + kw) * UB + w * 512 + lane * 16;
+    // per-lane copy plan: every lane its 16-byte code chunk (FP8: 32 bytes,
+    // two copies); lanes 8..15 the int5 high words; lanes 16..17 the scale pairs
+    const bool f8 = ST == STAGE8 && codec == 8;
+    const int ch = f8 ? 32 : 16;                     // code bytes per lane
+    const int sco = f8 ? SC8 : 640;                  // scale pairs in the stage
+    const uint8_t *src = P.packed + ((size_t)b * G + kw) * UB + w * 32 * ch + lane * ch;
     const size_t step = (size_t)KW * UB;
     const bool cp_hi = codec == 5 && lane >= 8 && lane < 16;
     const bool cp_sc = lane >= 16 && lane < 18;
-    const int ex_dst = cp_hi ? 512 + (lane - 8) * 16 : 640 + (lane - 16) * 16;
+    const int ex_dst = cp_hi ? 512 + (lane - 8) * 16 : sco + (lane - 16) * 16;
     const long ex_src = cp_hi ? (long)(NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
-                              : (long)(scale_off(codec) + w * 32 + (lane - 16) * 16) - (w * 512 + lane * 16);
+                              : (long)(scale_off(codec) + w * 32 + (lane - 16) * 16) - (w * 32 * ch + lane * ch);
     const bool cp_ex = cp_hi || cp_sc;
 
     // per-lane activation plan: token 8*nt + g, k = 64*grp + 16c
@@ -172,8 +191,9 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
     for (int r = 0; r < RING; ++r) {
         if (r < nj) {
             const uint8_t *sr = src + r * step;
-            cp_async16(ring + r * STAGE + lane * 16, sr);
-            if (cp_ex) cp_async16(ring + r * STAGE + ex_dst, sr + ex_src);
+            cp_async16(ring + r * ST + lane * ch, sr);
+            if (f8) cp_async16(ring + r * ST + lane * ch + 16, sr + 16);
+            if (cp_ex) cp_async16(ring + r * ST + ex_dst, sr + ex_src);
         }
         cp_async_commit();
     }
@@ -215,13 +235,15 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
                 }
                 cp_async_wait<RING - 1>();            // this group of every lane has landed
                 __syncwarp();
-                uint8_t *st = ring + r * STAGE;
-                const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * 16);
+                uint8_t *st = ring + r * ST;
+                const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * ch);
+                const uint4 cw8 = f8 ? *reinterpret_cast<const uint4 *>(st + lane * ch + 16) : make_uint4(0, 0, 0, 0);
                 const uint32_t hw = codec == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
-                const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + 640 + g * 4);
+                const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + sco + g * 4);
                 __syncwarp();                         // every lane has read the stage
                 if (j0 + r + RING < nj) {
-                    cp_async16(st + lane * 16, src_next);
+                    cp_async16(st + lane * ch, src_next);
+                    if (f8) cp_async16(st + lane * ch + 16, src_next + 16);
                     if (cp_ex) cp_async16(st + ex_dst, src_next + ex_src);
                     if (pf) {
 #pragma unroll
@@ -234,7 +256,8 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
                 x_cur += xstep;
 
                 uint32_t a[4][4];
-                decode_tile(codec, cw, hw, a);
+                if (f8) decode_tile8(cw, cw8, a);
+                else decode_tile(codec, cw, hw, a);
                 const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -286,8 +309,21 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
 template <int NJ, int RG, int NT>
 struct LineSmem {
     static constexpr int RED_STRIDE = 17;
-    __host__ __device__ static constexpr int rings(int kw) { return kw * RG * STAGE; }
-    __host__ __device__ static constexpr int bytes(int kw) { return rings(kw) + kw * NT * 8 * RED_STRIDE * 4; }
+    // st: the stage size of the CTA's codec (the launch sizes for the largest)
+    __host__ __device__ static constexpr int rings(int kw, int st) { return kw * RG * st; }
+    __host__ __device__ static constexpr int bytes(int kw, int st) {
+        return rings(kw, st) + kw * NT * 8 * RED_STRIDE * 4;
+    }
+};
+
+// Stage geometry of a codec, by its unit size: code bytes per lane, the
+// offset of the scale pairs, the stage size.
+template <int UB>
+struct LineStage {
+    static constexpr bool F8 = UB == UNIT8;
+    static constexpr int CH = F8 ? 32 : 16;
+    static constexpr int SC = F8 ? SC8 : 640;
+    static constexpr int BYTES = F8 ? STAGE8 : STAGE;
 };
 
 // Activation fragment of group R for token row pointer xr: the lane's 16 k.
@@ -311,8 +347,10 @@ struct LaneCopies {
 
 template <int UB, int RG, int R>
 __device__ __forceinline__ void issue_group(uint8_t *ring, const LaneCopies &lc, int lane) {
-    uint8_t *st = ring + (R % RG) * STAGE;
-    cp_async16(st + lane * 16, lc.src + R * UB);
+    using S = LineStage<UB>;
+    uint8_t *st = ring + (R % RG) * S::BYTES;
+    cp_async16(st + lane * S::CH, lc.src + R * UB);
+    if (S::F8) cp_async16(st + lane * S::CH + 16, lc.src + R * UB + 16);
     if (lc.ex) cp_async16(st + lc.ex_dst, lc.src + R * UB + lc.ex_src);
     cp_async_commit();
 }
@@ -330,7 +368,8 @@ template <int NT, int CODEC, int NJ, int RG, int XP, int R>
 __device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, int lane, int g,
                                            const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[XP][8],
                                            float (&acc)[NT][4]) {
-    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    constexpr int UB = unit_bytes(CODEC);
+    using S = LineStage<UB>;
     constexpr int ISSUED = RG + R < NJ ? RG + R : NJ;     // groups whose copies are issued
     uint32_t xb[NT][8];
     if (XP == NJ) {
@@ -342,16 +381,18 @@ __device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, 
     }
     cp_async_wait<ISSUED - 1 - R>();                   // groups 0..R of this lane have landed
     __syncwarp();                                      // ... and of every lane
-    const uint8_t *st = ring + (R % RG) * STAGE;
-    const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * 16);
+    const uint8_t *st = ring + (R % RG) * S::BYTES;
+    const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * S::CH);
+    const uint4 cw8 = S::F8 ? *reinterpret_cast<const uint4 *>(st + lane * S::CH + 16) : make_uint4(0, 0, 0, 0);
     const uint32_t hw = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
-    const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + 640 + g * 4);
+    const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + S::SC + g * 4);
     if (R + RG < NJ) {
         __syncwarp();                                  // every lane has read the stage
         issue_group<UB, RG, R + RG>(ring, lc, lane);
     }
     uint32_t a[4][4];
-    decode_tile(CODEC, cw, hw, a);
+    if (S::F8) decode_tile8(cw, cw8, a);
+    else decode_tile(CODEC, cw, hw, a);
     const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -385,7 +426,8 @@ template <int NT, int CODEC, int NJ, int RG>
 __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyParent &P, int tile, uint8_t *smem) {
     constexpr int RS = LineSmem<NJ, RG, NT>::RED_STRIDE;
     constexpr int T8 = 8 * NT;
-    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    constexpr int UB = unit_bytes(CODEC);
+    using S = LineStage<UB>;
     constexpr int XP = (NT == 1 && NJ <= 8) ? NJ : 1;   // activation fragments loaded up front
     const int KW = blockDim.x >> 5;
     const int b = tile / TILES, w = tile % TILES;
@@ -394,18 +436,20 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
     const int g = lane >> 2, c = lane & 3;
     const int T = args.T;
     const int gb = kw * NJ;                           // this warp's first group
-    uint8_t *ring = smem + kw * RG * STAGE;
-    float *red = reinterpret_cast<float *>(smem + LineSmem<NJ, RG, NT>::rings(KW));
+    uint8_t *ring = smem + kw * RG * S::BYTES;
+    float *red = reinterpret_cast<float *>(smem + LineSmem<NJ, RG, NT>::rings(KW, S::BYTES));
 
     // per-lane copy plan (as the ring kernel's): every lane its 16-byte code
-    // chunk; lanes 8..15 the int5 high words; lanes 16..17 the scale pairs
+    // chunk (FP8: 32 bytes); lanes 8..15 the int5 high words; lanes 16..17 the
+    // scale pairs
     const bool cp_hi = CODEC == 5 && lane >= 8 && lane < 16;
+    const int own = w * 32 * S::CH + lane * S::CH;    // the lane's chunk in the unit
     LaneCopies lc;
-    lc.src = P.packed + ((size_t)b * G + gb) * UB + w * 512 + lane * 16;
+    lc.src = P.packed + ((size_t)b * G + gb) * UB + own;
     lc.ex = cp_hi || (lane >= 16 && lane < 18);
-    lc.ex_dst = cp_hi ? 512 + (lane - 8) * 16 : 640 + (lane - 16) * 16;
-    lc.ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
-                      : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - (w * 512 + lane * 16);
+    lc.ex_dst = cp_hi ? 512 + (lane - 8) * 16 : S::SC + (lane - 16) * 16;
+    lc.ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - own
+                      : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - own;
     issue_groups<UB, RG>(std::make_integer_sequence<int, RG>{}, ring, lc, lane);
     // Programmatic dependent launch: with one token tile the next kernel in the
     // stream may start once this CTA's weight copies are issued and the
@@ -458,7 +502,10 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
     write_tile<RS>(P, red, T8, KW, tile, T);
 }
 
-template <int NT, int NJ, int RG>
+// F8: the launch has FP8 parents (the kernel then also serves the integer
+// codecs, for multi-parent launches); the integer-only instantiation keeps
+// the code of the integer codecs alone.
+template <int NT, int NJ, int RG, bool F8>
 __global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_constant__ SkinnyArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
     int pi = 0;
@@ -467,35 +514,37 @@ __global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_const
         if (i < args.nparents && (int)blockIdx.x >= args.p[i].cta_begin) pi = i;
     const SkinnyParent &P = args.p[pi];
     const int tile = blockIdx.x - P.cta_begin;
-    if (P.codec == 4) line_tile<NT, 4, NJ, RG>(args, P, tile, smem);
+    if (F8 && P.codec == 8) line_tile<NT, 8, NJ, RG>(args, P, tile, smem);
+    else if (P.codec == 4) line_tile<NT, 4, NJ, RG>(args, P, tile, smem);
     else line_tile<NT, 5, NJ, RG>(args, P, tile, smem);
 }
 
-template <int NT, int NJ, int RG>
+template <int NT, int NJ, int RG, bool F8>
 static cudaError_t launch_line_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
     static bool done[64] = {};
+    constexpr int ST = F8 ? STAGE8 : STAGE;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int kw = a.G / NJ;
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(skinny_line_kernel<NT, NJ, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 LineSmem<NJ, RG, NT>::bytes(16));
+        e = cudaFuncSetAttribute(skinny_line_kernel<NT, NJ, RG, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 LineSmem<NJ, RG, NT>::bytes(16, ST));
         if (e != cudaSuccess) return e;
         done[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kw * 32, 1, 1);
-    cfg.dynamicSmemBytes = LineSmem<NJ, RG, NT>::bytes(kw);
+    cfg.dynamicSmemBytes = LineSmem<NJ, RG, NT>::bytes(kw, ST);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, skinny_line_kernel<NT, NJ, RG>, a);
+    e = cudaLaunchKernelEx(&cfg, skinny_line_kernel<NT, NJ, RG, F8>, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -509,71 +558,84 @@ int skinny_line_groups(int G, int nj_pref) {
     return 0;
 }
 
-cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream) {
+template <bool F8>
+static cudaError_t launch_line_f(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream) {
     if (nj == 16 && a.G % 16 == 0 && a.G / 16 <= 16) {
         switch (nt) {
-            case 1: return launch_line_t<1, 16, 8>(a, grid, pdl, stream);
-            case 2: return launch_line_t<2, 16, 8>(a, grid, pdl, stream);
-            case 4: return launch_line_t<4, 16, 8>(a, grid, pdl, stream);
+            case 1: return launch_line_t<1, 16, 8, F8>(a, grid, pdl, stream);
+            case 2: return launch_line_t<2, 16, 8, F8>(a, grid, pdl, stream);
+            case 4: return launch_line_t<4, 16, 8, F8>(a, grid, pdl, stream);
         }
     } else if (nj == 8 && a.G % 8 == 0 && a.G / 8 <= 16) {
         switch (nt) {
-            case 1: return launch_line_t<1, 8, 8>(a, grid, pdl, stream);
-            case 2: return launch_line_t<2, 8, 8>(a, grid, pdl, stream);
-            case 4: return launch_line_t<4, 8, 8>(a, grid, pdl, stream);
+            case 1: return launch_line_t<1, 8, 8, F8>(a, grid, pdl, stream);
+            case 2: return launch_line_t<2, 8, 8, F8>(a, grid, pdl, stream);
+            case 4: return launch_line_t<4, 8, 8, F8>(a, grid, pdl, stream);
         }
     }
     return cudaErrorInvalidValue;
 }
 
-template <int NT, int KW>
+cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, bool f8,
+                               cudaStream_t stream) {
+    return f8 ? launch_line_f<true>(a, nt, nj, grid, pdl, stream) : launch_line_f<false>(a, nt, nj, grid, pdl, stream);
+}
+
+template <int NT, int KW, int ST>
 static cudaError_t prepare(int dev) {
     static bool done[64] = {};
     if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NT, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SkinnySmem<NT, KW>::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NT, KW, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SkinnySmem<NT, KW, ST>::BYTES);
     if (e != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
 
-template <int NT, int KW>
+template <int NT, int KW, int ST>
 static cudaError_t launch_skinny_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if ((e = prepare<NT, KW>(dev)) != cudaSuccess) return e;
+    if ((e = prepare<NT, KW, ST>(dev)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(KW * 32, 1, 1);
-    cfg.dynamicSmemBytes = SkinnySmem<NT, KW>::BYTES;
+    cfg.dynamicSmemBytes = SkinnySmem<NT, KW, ST>::BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, skinny_kernel<NT, KW>, a);
+    e = cudaLaunchKernelEx(&cfg, skinny_kernel<NT, KW, ST>, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Tokens per launch: 8 * nt with nt in {1, 2, 4}; kw warps per CTA in {4, 8}.
-cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream) {
+template <int ST>
+static cudaError_t launch_skinny_s(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, cudaStream_t stream) {
     if (kw == 8) {
         switch (nt) {
-            case 1: return launch_skinny_t<1, 8>(a, grid, pdl, stream);
-            case 2: return launch_skinny_t<2, 8>(a, grid, pdl, stream);
-            case 4: return launch_skinny_t<4, 8>(a, grid, pdl, stream);
+            case 1: return launch_skinny_t<1, 8, ST>(a, grid, pdl, stream);
+            case 2: return launch_skinny_t<2, 8, ST>(a, grid, pdl, stream);
+            case 4: return launch_skinny_t<4, 8, ST>(a, grid, pdl, stream);
         }
     } else if (kw == 4) {
         switch (nt) {
-            case 1: return launch_skinny_t<1, 4>(a, grid, pdl, stream);
-            case 2: return launch_skinny_t<2, 4>(a, grid, pdl, stream);
-            case 4: return launch_skinny_t<4, 4>(a, grid, pdl, stream);
+            case 1: return launch_skinny_t<1, 4, ST>(a, grid, pdl, stream);
+            case 2: return launch_skinny_t<2, 4, ST>(a, grid, pdl, stream);
+            case 4: return launch_skinny_t<4, 4, ST>(a, grid, pdl, stream);
         }
     }
     return cudaErrorInvalidValue;
+}
+
+// Tokens per launch: 8 * nt with nt in {1, 2, 4}; kw warps per CTA in {4, 8};
+// f8: some parent holds FP8 codes (larger stages).
+cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, bool f8, cudaStream_t stream) {
+    return f8 ? launch_skinny_s<STAGE8>(a, nt, kw, grid, pdl, stream)
+              : launch_skinny_s<STAGE>(a, nt, kw, grid, pdl, stream);
 }
 
 }  // namespace qg

@@ -221,6 +221,8 @@ CONFIGS = {
     # 5120) as a SwiGLU pair of two 17408-row matrices (parents 0 and 1)
     "linear_add": dict(parents=[(5120, 5)], K=6144, Ts=[1, 2, 4, 8], outliers=True, epilogue="add"),
     "swiglu": dict(parents=[(17408, 4), (17408, 4)], K=5120, Ts=[1, 2, 4, 8], outliers=True, epilogue="swiglu"),
+    # the decode shape with FP8 (E4M3) weights at decode and verify widths
+    "decode_fp8": dict(parents=[(5120, 8)], K=6144, Ts=[1, 2, 4, 8], outliers=True),
 }
 
 

@@ -16,7 +16,7 @@
  *
  * Number formats
  *   q  symmetric two's-complement code, no zero point: int4 in [-8, 7],
- *      int5 in [-16, 15];
+ *      int5 in [-16, 15]; or an FP8 E4M3 value (below), exact in bf16;
  *   s  IEEE fp16, one per (row, 64-column group); any finite value, negative
  *      and subnormal included (non-finite scales propagate but the result is
  *      then unspecified beyond being non-finite);
@@ -30,6 +30,13 @@
  *         code 2j+1 in bits 4-7.
  *   int5: 5K/8 bytes per row, row-major; LSB-first bitstream, code k in bits
  *         5k .. 5k+4.
+ *   fp8:  K bytes per row, row-major; byte k is the OCP FP8 E4M3 code of
+ *         column k (bias 7, subnormals, no infinities; the NaN codes S.1111.111
+ *         are outside the codec and give unspecified results), weighted by the
+ *         same fp16 scale per 64 columns.  FP8 is the weight-only FP8 format
+ *         of the FP8-weight kernel the "Speculative decoding" page checks at
+ *         verify widths; it is served on the small-T routes, so an FP8 plan's
+ *         T_max is at most 32.
  *   scales: fp16 bit patterns, row-major [N][K/64].
  *
  * Conventions for every call
@@ -69,7 +76,7 @@ typedef enum {
     QGEMM_ERR_UNSUPPORTED = 8      /* no usable GPU of the architecture this library was built for */
 } qgemm_status;
 
-typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5 } qgemm_codec;
+typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5, QGEMM_FP8 = 8 } qgemm_codec;
 
 typedef struct qgemm_plan_s *qgemm_plan_t;
 
@@ -104,6 +111,7 @@ qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
  * "ninfer-3080 docs/performance.md" route boundaries section explains why
  * boundaries must come from measurement).  Queries the current device's SM
  * count; launches nothing.  *out must be released with qgemm_plan_destroy.
+ * QGEMM_ERR_T_OUT_OF_DOMAIN for an FP8 plan with T_max > 32.
  */
 qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out);
 

@@ -52,6 +52,7 @@ WORKLOADS = {
     "linear_add": ("linear_add", [1, 2, 4, 8]),
     "swiglu": ("swiglu", [1, 2, 4, 8]),
     "decode_fp8": ("decode_fp8", [1, 2, 4, 8]),
+    "prefill_fp8": ("prefill_fp8", [256, 1024, 4096]),
 }
 
 

@@ -109,9 +109,6 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5 || c == QGEMM_FP8; }
 
-// FP8 weights are served on the small-T routes only (token tiles up to 32).
-constexpr int FP8_T_MAX = 32;
-
 extern "C" {
 
 const char *qgemm_status_string(qgemm_status st) {
@@ -157,7 +154,6 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     *out = nullptr;
     if (!valid_codec(codec) || T_max < 1) return QGEMM_ERR_INVALID_ARG;
     if (N < 1 || K < GROUP || K % GROUP) return QGEMM_ERR_SHAPE;
-    if (codec == QGEMM_FP8 && T_max > FP8_T_MAX) return QGEMM_ERR_T_OUT_OF_DOMAIN;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
@@ -305,8 +301,6 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     unsigned int *status = status_ptr();
     if (!status) return QGEMM_ERR_CUDA;
     if (route == ROUTE_WIDE128) {
-        for (int i = 0; i < np; ++i)
-            if (plans[i]->codec == QGEMM_FP8) return QGEMM_ERR_T_OUT_OF_DOMAIN;   // small-T routes only
         WideParent wp[MAX_PARENTS];
         memset(wp, 0, sizeof wp);
         for (int i = 0; i < np; ++i) {

@@ -256,7 +256,12 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const int my_tiles = (int)blockIdx.x < args.ntiles ? (args.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int steps = my_tiles * G;
     constexpr int codec = CODEC;
-    constexpr int UB = CODEC == 5 ? UNIT5 : UNIT4;
+    constexpr int UB = unit_bytes(CODEC);
+    // weight stages: pairs of units; FP8 units are larger, so the same region
+    // holds fewer pairs
+    constexpr int WSLOT = 2 * UB;
+    constexpr int nwp = (NWP * 2 * UNIT5) / WSLOT < NWP ? (NWP * 2 * UNIT5) / WSLOT : NWP;
+    static_assert(nwp >= 2, "weight ring");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -285,12 +290,12 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
             const uint8_t *units = tr.P->packed + (size_t)tr.blk * G * UB;
             for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
-                const int wsl = jp % NWP;
+                const int wsl = jp % nwp;
                 const uint32_t bytes = (2 * j + 1 < G ? 2 : 1) * UB;
-                if (jp >= NWP && !(ok = mbar_wait_warp(&w_empty[wsl], ((jp / NWP) - 1) & 1, args.status))) break;
+                if (jp >= nwp && !(ok = mbar_wait_warp(&w_empty[wsl], ((jp / nwp) - 1) & 1, args.status))) break;
                 if (elect_one()) {
                     mbar_arrive_expect_tx(&w_full[wsl], bytes);
-                    bulk_g2s(ws + wsl * 2 * UNIT5, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
+                    bulk_g2s(ws + wsl * WSLOT, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
                 }
                 __syncwarp();
             }
@@ -353,12 +358,39 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
                 const int g0 = it * G + 2 * j;        // step of the pair's first group
                 const bool two = 2 * j + 1 < G;
-                const int wsl = jp % NWP;
-                if (!(ok = mbar_wait_warp(&w_full[wsl], (jp / NWP) & 1, args.status))) break;
+                const int wsl = jp % nwp;
+                if (!(ok = mbar_wait_warp(&w_full[wsl], (jp / nwp) & 1, args.status))) break;
+                uint32_t av[2][32];
+                if constexpr (CODEC == 8) {
+                    // E4M3: the row's 16 codes of lane chunk c (k 16c .. 16c+15)
+                    // decoded straight from shared memory, in natural k order
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint8_t *u = ws + wsl * WSLOT + e * UB;
+                        if (e == 0 || two) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(u + tile * 1024 + (4 * gi_ + c) * 32 + 16 * half);
+                                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int j2 = 0; j2 < 4; ++j2) {
+                                    av[e][8 * c + 2 * j2] = dec8_pair<0>(wv[j2]);
+                                    av[e][8 * c + 2 * j2 + 1] = dec8_pair<1>(wv[j2]);
+                                }
+                            }
+                            sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
+                        } else {
+#pragma unroll
+                            for (int m = 0; m < 32; ++m) av[e][m] = 0u;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[wsl]);
+                } else {
                 uint32_t wd[2][8], hw[2][4];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const uint8_t *u = ws + wsl * 2 * UNIT5 + e * UB;
+                    const uint8_t *u = ws + wsl * WSLOT + e * UB;
                     if (e == 0 || two) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
@@ -377,7 +409,6 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[wsl]);
                 // decode to 32 bf16x2 words per group in natural k order: word m = (k 2m, 2m+1)
-                uint32_t av[2][32];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
 #pragma unroll
@@ -396,6 +427,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                             }
                         }
                     }
+                }
                 }
                 // the A stages of both groups are free once the MMAs of steps
                 // g0 - NA and g0 + 1 - NA have completed
@@ -588,10 +620,10 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
     CUtensorMap xmap;
     cudaError_t e = make_xmap(&xmap, X, T, K);
     if (e != cudaSuccess) return e;
-    int n4 = 0, n5 = 0;
+    int n4 = 0, n5 = 0, n8 = 0;
     bool fused = false;
     for (int i = 0; i < np; ++i) {
-        (parents[i].codec == 4 ? n4 : n5)++;
+        (parents[i].codec == 4 ? n4 : parents[i].codec == 5 ? n5 : n8)++;
         fused = fused || parents[i].epi != EPI_STORE || parents[i].ybf16;
     }
     if (n4 && (e = fused ? launch_codec<4, true>(parents, np, xmap, T, K, status, stream)
@@ -600,7 +632,10 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
     if (n5 && (e = fused ? launch_codec<5, true>(parents, np, xmap, T, K, status, stream)
                          : launch_codec<5, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
         return e;
-    *launches = (n4 > 0) + (n5 > 0);
+    if (n8 && (e = fused ? launch_codec<8, true>(parents, np, xmap, T, K, status, stream)
+                         : launch_codec<8, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
+        return e;
+    *launches = (n4 > 0) + (n5 > 0) + (n8 > 0);
     return cudaSuccess;
 }
 

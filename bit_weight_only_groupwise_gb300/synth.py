@@ -223,6 +223,7 @@ CONFIGS = {
     "swiglu": dict(parents=[(17408, 4), (17408, 4)], K=5120, Ts=[1, 2, 4, 8], outliers=True, epilogue="swiglu"),
     # the decode shape with FP8 (E4M3) weights at decode and verify widths
     "decode_fp8": dict(parents=[(5120, 8)], K=6144, Ts=[1, 2, 4, 8], outliers=True),
+    "prefill_fp8": dict(parents=[(7168, 8)], K=5120, Ts=[256, 1024, 4096], outliers=True),
 }
 
 

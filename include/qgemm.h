@@ -35,8 +35,7 @@
  *         are outside the codec and give unspecified results), weighted by the
  *         same fp16 scale per 64 columns.  FP8 is the weight-only FP8 format
  *         of the FP8-weight kernel the "Speculative decoding" page checks at
- *         verify widths; it is served on the small-T routes, so an FP8 plan's
- *         T_max is at most 32.
+ *         verify widths; every route serves it.
  *   scales: fp16 bit patterns, row-major [N][K/64].
  *
  * Conventions for every call
@@ -111,7 +110,6 @@ qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
  * "ninfer-3080 docs/performance.md" route boundaries section explains why
  * boundaries must come from measurement).  Queries the current device's SM
  * count; launches nothing.  *out must be released with qgemm_plan_destroy.
- * QGEMM_ERR_T_OUT_OF_DOMAIN for an FP8 plan with T_max > 32.
  */
 qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out);
 

@@ -1,11 +1,11 @@
 """GPU parity of the FP8 (E4M3) weight codec against the fp64 oracle.
 
-FP8 plans run on the small-T routes (token tiles of 8, 16 and 32): the
-straight-line kernel where K/64 is a multiple of 8 (up to 16 warps), the ring
-kernel otherwise.  Checked here: every finite code decodes exactly (one-hot
-activations return s * value bitwise, subnormal codes included), parity on
-every small-T route and both kernels, ragged N, a multi-parent launch mixing
-FP8 with int4, the fused outputs on FP8 weights, and the T_max limit.
+Checked on every route: the small-T token tiles of 8, 16 and 32 (the
+straight-line kernel where K/64 is a multiple of 8, the ring kernel
+otherwise) and the tcgen05 tiles.  Every finite code decodes exactly (one-hot
+activations return s * value bitwise, subnormal codes included, on both
+kinds of route), parity at every width, ragged N, multi-parent launches
+mixing FP8 with int4, and the fused outputs on FP8 weights.
 """
 import numpy as np
 import pytest
@@ -39,30 +39,32 @@ def _status_clean():
     assert qg.qgemm_device_status(clear=True) == qg.QGEMM_OK
 
 
-def test_every_code_decodes_exactly():
+@pytest.mark.parametrize("tw", [32, 128])
+def test_every_code_decodes_exactly(tw):
     # row n holds the finite codes in a rotated order; X = one-hot columns, so
-    # Y[t][n] = s[n][k/64] * value(code[n][k]) with k = column t: exact in fp32
+    # Y[t][n] = s[n][k/64] * value(code[n][k]) with k = column t: exact in fp32.
+    # tw = 32 runs the 32-token small-T tile, 128 the tcgen05 tile.
     N, K = 128, 512
     finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)        # 254 codes
     codes = np.stack([np.resize(np.roll(finite, 3 * n), K) for n in range(N)]).astype(np.uint8)
     scales = synth.group_scales(61, 1, N, K)
     p = {"bits": 8, "N": N, "K": K, "packed": codes, "scales": scales}
-    W = weights(p, T_max=32)
+    W = weights(p, T_max=tw)
     ref_w = oracle.dequant(8, codes, scales, N, K)
-    for k0 in range(0, K, 32):
-        ks = np.arange(k0, k0 + 32)
-        x = np.zeros((32, K), np.uint16)
-        x[np.arange(32), ks] = 0x3F80                       # bf16 1.0
+    for k0 in range(0, K, tw):
+        ks = np.arange(k0, k0 + tw)
+        x = np.zeros((tw, K), np.uint16)
+        x[np.arange(tw), ks] = 0x3F80                       # bf16 1.0
         Y = host(W.run(dev_x(x)))
-        assert np.array_equal(Y, ref_w[:, ks].T), f"columns {k0}..{k0 + 31}"
+        assert np.array_equal(Y, ref_w[:, ks].T), f"columns {k0}..{k0 + tw - 1} ({W.route(tw)})"
 
 
-@pytest.mark.parametrize("T", [1, 3, 8, 13, 16, 24, 32])
+@pytest.mark.parametrize("T", [1, 3, 8, 13, 16, 24, 32, 33, 100, 300])
 @pytest.mark.parametrize("N,K", [(5120, 6144), (1000, 1024), (130, 576), (300, 9216)])
 def test_parity(T, N, K):
-    # K = 576 (9 groups) and 9216 (144 groups) take the ring kernel
+    # K = 576 (9 groups) and 9216 (144 groups) take the ring kernel at T <= 32
     p = synth.weights(62, N, K, 8)
-    W = weights(p, T_max=32)
+    W = weights(p, T_max=512)
     x = synth.activations(62, T, K, outliers=True)
     Y = W.run(dev_x(x))
     Yref, A = oracle.gemm_parent(p, x)
@@ -79,12 +81,13 @@ def test_repeatable(T):
         assert torch.equal(W.run(X), y0)
 
 
-@pytest.mark.parametrize("T", [4, 16])
+@pytest.mark.parametrize("T", [4, 16, 64])
 def test_multi_parent_with_int4(T):
+    # at T = 64 (tcgen05) the two codecs take one launch each
     K = 5120
     pf = synth.weights(64, 4096, K, 8, parent=0)
     pi = synth.weights(64, 1024, K, 4, parent=1)
-    ws = [weights(pf, T_max=32), weights(pi, T_max=32)]
+    ws = [weights(pf, T_max=64), weights(pi, T_max=64)]
     x = synth.activations(64, T, K, outliers=True)
     Ys = qg.run_multi(ws, dev_x(x))
     for p, Y in zip((pf, pi), Ys):
@@ -92,29 +95,24 @@ def test_multi_parent_with_int4(T):
         assert_close(host(Y), Yref, A, f"multi int{p['bits']} T={T}")
 
 
-@pytest.mark.parametrize("T", [1, 8, 30])
+@pytest.mark.parametrize("T", [1, 8, 30, 100])
 def test_fused_outputs(T):
     K = 1024
     # residual add
     p = synth.weights(65, 700, K, 8)
     x = synth.activations(65, T, K, outliers=True)
     R = np.random.default_rng(T).normal(0, 4, (T, 700)).astype(np.float32)
-    W = weights(p, T_max=32, epilogue=qg.QGEMM_EPILOGUE_ADD)
+    W = weights(p, T_max=128, epilogue=qg.QGEMM_EPILOGUE_ADD)
     Y = W.run(dev_x(x), R=torch.from_numpy(R).cuda())
     Yref, A = oracle.linear_add(8, p["packed"], p["scales"], x, R, 700, K)
     assert_close(host(Y), Yref, A, f"fp8 add T={T}")
     # SwiGLU pair
     gate, up = synth.weights(66, 203, K, 8, parent=0), synth.weights(66, 203, K, 8, parent=1)
-    P = qg.SwiGLUPair(8, 203, K, gate["packed"], gate["scales"], up["packed"], up["scales"], T_max=32)
+    P = qg.SwiGLUPair(8, 203, K, gate["packed"], gate["scales"], up["packed"], up["scales"], T_max=128)
     Ys = P.run(dev_x(x))
     out, g, u, Ag, Au = oracle.swiglu_pair(gate, up, x)
     assert_close_swiglu(host(Ys), out, g, u, Ag, Au, f"fp8 swiglu T={T}")
 
 
-def test_width_limit():
-    st, h = qg.qgemm_plan(256, 512, qg.QGEMM_FP8, 33)
-    assert st == qg.QGEMM_ERR_T_OUT_OF_DOMAIN and not h
-    st, h = qg.qgemm_plan(256, 512, qg.QGEMM_FP8, 32)
-    assert st == qg.QGEMM_OK
-    qg.qgemm_plan_destroy(h)
+def test_packed_size():
     assert qg.qgemm_packed_bytes(256, 512, qg.QGEMM_FP8) == 2 * (8192 + 256) * 8

@@ -46,7 +46,7 @@ EXPORTS = [
     "qgemm_plan_workspace_bytes", "qgemm_plan_bind", "qgemm_run", "qgemm_run_multi",
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
     "qgemm_device_status", "qgemm_plan_set_pdl", "qgemm_pair_packed_bytes", "qgemm_pack_pair",
-    "qgemm_plan_set_epilogue", "qgemm_run_ex",
+    "qgemm_plan_set_epilogue", "qgemm_run_ex", "qgemm_selftest_timeout",
 ]
 
 _lock = threading.Lock()
@@ -81,6 +81,7 @@ def _declare(lib):
         "qgemm_pack_pair": ([i32, i32, i32, vp, vp, vp, vp, vp, vp], i32),
         "qgemm_plan_set_epilogue": ([vp, i32, i32], i32),
         "qgemm_run_ex": ([vp, vp, i32, vp, vp, vp], i32),
+        "qgemm_selftest_timeout": ([vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -200,6 +201,10 @@ def qgemm_route_name(route: int) -> str:
 
 def qgemm_launch_count() -> int:
     return load().qgemm_launch_count()
+
+
+def qgemm_selftest_timeout(stream=None) -> int:
+    return load().qgemm_selftest_timeout(_stream(stream))
 
 
 def qgemm_device_status(stream=None, clear: bool = False) -> int:

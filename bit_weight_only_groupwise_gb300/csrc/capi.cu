@@ -13,6 +13,7 @@ namespace qg {
 cudaError_t launch_pack(int codec, int N, int K, const void *canon, const uint16_t *scales, void *out,
                         cudaStream_t stream);
 cudaError_t launch_fence(cudaStream_t stream);
+cudaError_t launch_wait_timeout(unsigned int *status, int tries, cudaStream_t stream);
 cudaError_t launch_pack_pair(int codec, int F, int K, const void *gate, const uint16_t *gate_scales,
                              const void *up, const uint16_t *up_scales, void *out, cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, bool f8, cudaStream_t stream);
@@ -248,6 +249,14 @@ const char *qgemm_route_name(int route) {
 }
 
 uint64_t qgemm_launch_count(void) { return g_launches.load(); }
+
+qgemm_status qgemm_selftest_timeout(qgemm_stream_t stream) {
+    unsigned int *status = status_ptr();
+    if (!status) return QGEMM_ERR_CUDA;
+    if (launch_wait_timeout(status, 16, (cudaStream_t)stream) != cudaSuccess) return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return QGEMM_OK;
+}
 
 qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear) {
     unsigned int v = 0;

@@ -118,6 +118,23 @@ cudaError_t launch_pack_pair(int codec, int F, int K, const void *gate, const ui
 
 __global__ void fence_kernel() {}
 
+// Diagnostic: one bounded wait on an mbarrier that nothing arrives at, the
+// path every kernel takes when a wait runs out (device status set to
+// timeout, the thread returns).  `tries` suspending tests of at most ~20 us.
+__global__ void wait_timeout_kernel(unsigned int *status, int tries) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait_limit(&bar, 0, status, tries);
+    }
+}
+
+cudaError_t launch_wait_timeout(unsigned int *status, int tries, cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(status, tries);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fence(cudaStream_t stream) {
     fence_kernel<<<1, 32, 0, stream>>>();
     return cudaGetLastError();

@@ -187,12 +187,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // status set to timeout) if it did not complete within SPIN_LIMIT tries.  A
 // phase that has already completed is seen by the non-blocking test, which
 // is cheaper than the suspending form.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, unsigned int *status,
+                                                long long limit) {
     if (mbar_test(bar, parity)) return true;
-    for (long long i = 0; i < SPIN_LIMIT; ++i)
+    for (long long i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicExch(status, 7u /* QGEMM_ERR_TIMEOUT */);
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status) {
+    return mbar_wait_limit(bar, parity, status, SPIN_LIMIT);
 }
 
 // One lane of a converged warp: true in exactly one lane.

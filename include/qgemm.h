@@ -242,6 +242,16 @@ uint64_t qgemm_launch_count(void);
  */
 qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear);
 
+/*
+ * Diagnostic of the timeout path: launches one kernel whose single bounded
+ * wait is on a barrier nothing completes, so that it runs out after a few
+ * hundred microseconds and sets the device status word to QGEMM_ERR_TIMEOUT,
+ * as any kernel does when one of its waits runs out.  The kernel faults
+ * nothing and leaves the context usable; read and clear the word with
+ * qgemm_device_status.  Returns QGEMM_ERR_CUDA if the launch fails.
+ */
+qgemm_status qgemm_selftest_timeout(qgemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,4 +1,4 @@
-"""Groupwise int4/int5 weight-only dequant-GEMM for GB300 (sm_103a).
+"""Groupwise int4/int5/FP8 weight-only dequant-GEMM for GB300 (sm_103a).
 
 Python binding of the C-ABI library ``_lib/libqgemm.so`` (declared in
 ``include/qgemm.h``).  Every function here has the name of the C entry point
@@ -230,8 +230,10 @@ class GroupwiseWeights:
     """One packed weight matrix bound to a plan (device memory from torch).
 
     ``codes_canonical`` and ``scales_fp16`` are the canonical packed codes
-    (uint8 [N, row_bytes]) and fp16 bit patterns (uint16/int16 [N, K/64]), as
-    numpy arrays or torch tensors on the host or the device.
+    (uint8 [N, row_bytes]: K/2 bytes per row for int4, 5K/8 for int5, K for
+    FP8) and fp16 bit patterns (uint16/int16 [N, K/64]), as numpy arrays or
+    torch tensors on the host or the device.  ``epilogue`` and ``out`` select
+    a fused output (residual add) and the output type (fp32 or bf16).
     """
 
     def __init__(self, codec: int, N: int, K: int, codes_canonical, scales_fp16, T_max: int,

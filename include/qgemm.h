@@ -1,5 +1,5 @@
 /*
- * qgemm -- groupwise int4/int5 weight-only dequant-GEMM for GB300 (sm_103a).
+ * qgemm -- groupwise int4/int5/FP8 weight-only dequant-GEMM for GB300 (sm_103a).
  *
  *     Y[t][n] = sum_k X[t][k] * deq(W)[n][k],   deq(W)[n][k] = s[n][k/64] * q[n][k]
  *

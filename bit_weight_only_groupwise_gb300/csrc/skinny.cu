@@ -34,6 +34,7 @@
 //   (the pages name ramp and drain at kernel boundaries as what is left at
 //   one stream).  Where the next kernel may start is measured per kernel:
 //   see the trigger placements below.
+#include <atomic>
 #include <utility>
 
 #include "qgemm_internal.cuh"
@@ -521,18 +522,18 @@ __global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_const
 
 template <int NT, int NJ, int RG, bool F8>
 static cudaError_t launch_line_t(const SkinnyArgs &a, int grid, bool pdl, cudaStream_t stream) {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];
     constexpr int ST = F8 ? STAGE8 : STAGE;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const int kw = a.G / NJ;
-    if (!done[dev]) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(skinny_line_kernel<NT, NJ, RG, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  LineSmem<NJ, RG, NT>::bytes(16, ST));
         if (e != cudaSuccess) return e;
-        done[dev] = true;
+        done[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -583,12 +584,12 @@ cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bo
 
 template <int NT, int KW, int ST>
 static cudaError_t prepare(int dev) {
-    static bool done[64] = {};
-    if (done[dev]) return cudaSuccess;
+    static std::atomic<bool> done[64];
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(skinny_kernel<NT, KW, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SkinnySmem<NT, KW, ST>::BYTES);
     if (e != cudaSuccess) return e;
-    done[dev] = true;
+    done[dev].store(true, std::memory_order_release);
     return cudaSuccess;
 }
 

@@ -39,6 +39,8 @@
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // to timeout and the CTA winds down (after a bounded pause that lets copies
 // and MMAs already issued land before tensor memory is released).
+#include <atomic>
+
 #include <cuda.h>
 
 #include "qgemm_internal.cuh"
@@ -539,19 +541,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up once (a function-local static: thread-safe initialisation).
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const EncodeTiledFn fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -575,18 +575,20 @@ int wide_tile_tokens() { return wide::BN; }
 template <int CODEC, bool FUSED>
 static cudaError_t launch_codec(const WideParent *parents, int np, const CUtensorMap &xmap, int T, int K,
                                 unsigned int *status, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    static int sms[64] = {};
+    static std::atomic<bool> attr_set[64];
+    static std::atomic<int> sms[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(wide_kernel<CODEC, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  wide::Smem::BYTES);
         if (e != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        attr_set[dev] = true;
+        int n = 0;
+        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        sms[dev].store(n, std::memory_order_relaxed);
+        attr_set[dev].store(true, std::memory_order_release);
     }
     WideArgs a;
     memset(&a, 0, sizeof a);
@@ -609,7 +611,8 @@ static cudaError_t launch_codec(const WideParent *parents, int np, const CUtenso
     a.status = status;
     // persistent: one CTA per SM (its shared memory allows no more), each
     // taking the tiles blockIdx.x, blockIdx.x + grid, ...
-    const int grid = tiles < sms[dev] ? tiles : sms[dev];
+    const int nsm = sms[dev].load(std::memory_order_relaxed);
+    const int grid = tiles < nsm ? tiles : nsm;
     wide_kernel<CODEC, FUSED><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
     return cudaGetLastError();
 }

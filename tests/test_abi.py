@@ -49,6 +49,14 @@ def test_host_only_entry_points(lib):
     assert qg.qgemm_packed_bytes(5120, 6144, qg.QGEMM_INT4) == 40 * 96 * 4352
     for bad in ((0, 64, 4), (16, 100, 4), (16, 0, 4), (16, 64, 6)):
         assert qg.qgemm_packed_bytes(*bad) == 0
+    # FP8 units: 8192 code bytes + 256 scale bytes
+    assert qg.qgemm_packed_bytes(256, 512, qg.QGEMM_FP8) == 2 * 8 * 8448
+    # a SwiGLU pair of F rows each packs as 16 * ceil(F / 8) rows
+    assert qg.qgemm_pair_packed_bytes(8, 512, qg.QGEMM_INT4) == qg.qgemm_packed_bytes(16, 512, qg.QGEMM_INT4)
+    assert qg.qgemm_pair_packed_bytes(17408, 5120, qg.QGEMM_INT4) == qg.qgemm_packed_bytes(34816, 5120, qg.QGEMM_INT4)
+    assert qg.qgemm_pair_packed_bytes(203, 64, qg.QGEMM_FP8) == qg.qgemm_packed_bytes(416, 64, qg.QGEMM_FP8)
+    for bad in ((0, 64, 4), (8, 100, 4), (8, 64, 7)):
+        assert qg.qgemm_pair_packed_bytes(*bad) == 0
     assert qg.qgemm_route_name(-1) == "none"
     assert qg.qgemm_launch_count() >= 0
 
@@ -65,6 +73,14 @@ def test_argument_errors_before_any_device_work(lib):
     assert qg.qgemm_pack_weights(qg.QGEMM_INT4, 16, 64, 16, 16, 8, 0) == qg.QGEMM_ERR_ALIGNMENT
     assert qg.qgemm_run(None, 16, 1, 16, 0) == qg.QGEMM_ERR_INVALID_ARG
     assert qg.qgemm_run_multi([], 16, 1, [], 0) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_run_ex(None, 16, 1, None, 16, 0) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_plan_set_epilogue(None, qg.QGEMM_EPILOGUE_ADD) == qg.QGEMM_ERR_INVALID_ARG
+    # the pair pack validates before launching anything
+    assert qg.qgemm_pack_pair(qg.QGEMM_INT4, 8, 64, 16, 16, None, 16, 16, 0) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_pack_pair(qg.QGEMM_INT4, 0, 64, 16, 16, 16, 16, 16, 0) == qg.QGEMM_ERR_SHAPE
+    assert qg.qgemm_pack_pair(qg.QGEMM_INT4, 8, 96, 16, 16, 16, 16, 16, 0) == qg.QGEMM_ERR_SHAPE
+    assert qg.qgemm_pack_pair(qg.QGEMM_FP8, 8, 64, 16, 16, 16, 16, 8, 0) == qg.QGEMM_ERR_ALIGNMENT
+    assert qg.qgemm_pack_pair(6, 8, 64, 16, 16, 16, 16, 16, 0) == qg.QGEMM_ERR_INVALID_ARG
     assert qg.qgemm_plan_destroy(None) == qg.QGEMM_OK
 
 

@@ -5,6 +5,8 @@ must report QGEMM_ERR_UNSUPPORTED instead of crashing.
 """
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -90,3 +92,18 @@ def test_plan_without_gpu_reports_unsupported(lib):
         pytest.skip("a GPU is present")
     st, plan = qg.qgemm_plan(256, 512, qg.QGEMM_INT4, 8)
     assert st == qg.QGEMM_ERR_UNSUPPORTED and not plan
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """A C99 program includes the header (-Wall -Werror), links every entry
+    point against the library and runs the host-only calls."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    exe = str(tmp_path / "abi_check")
+    libdir = os.path.dirname(qg.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_check.c"), "-o", exe, "-L", libdir, "-lqgemm",
+                    f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "abi ok", (out.returncode, out.stdout, out.stderr)

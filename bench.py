@@ -235,20 +235,53 @@ def oracle_sample(desc, seconds: float = 12.0):
     return done_bytes / elapsed / 1e9, elapsed, sample
 
 
+def oracle_rows(desc, wl, lib, r0: int, nrows: int):
+    """Time the oracle on rows [r0, r0 + nrows) (cyclic) of every parent at
+    every width of the step; returns (seconds, algorithmic bytes of that share
+    of the step).  Wide widths run on 8 columns and scale by (T+1)/9."""
+    import oracle
+    K = desc["K"]
+    elapsed, done = 0.0, 0.0
+    for T in desc["T"]:
+        cols = min(T, 8)
+        x = wl["x"][:cols]
+        for p in wl["parents"]:
+            N = p["N"]
+            n = min(nrows, N)
+            idx = (r0 + np.arange(n)) % N
+            t0 = time.perf_counter()
+            oracle.gemm(p["bits"], p["packed"][idx], p["scales"][idx], x, n, K, lib=lib)
+            elapsed += (time.perf_counter() - t0) * (T + 1) / (cols + 1)
+            done += weight_bytes(n, K, p["bits"]) + 2 * T * K * n / N
+    return elapsed, done
+
+
 def run_reference(args, desc):
+    """The fp64 oracle on the host cores, as it stands: each step times it on
+    a slice of the weight rows (every parent, every width), sized so that the
+    whole --warmup + --steps run takes about --ref-seconds; the value is the
+    median over the timed steps of the slice's algorithmic bytes per second."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
-    oracle.load()
-    per_step = []
+    lib = oracle.load()
+    wl = synth.workload(WORKLOADS[desc["name"]][0], max(desc["T"]))
+    n_steps = args.warmup + args.steps
+    # calibrate: seconds per weight row of a step
+    t_cal, _ = oracle_rows(desc, wl, lib, 0, 32)
+    per_row = max(t_cal / 32, 1e-7)
+    rows = int(max(1, min(max(p["N"] for p in wl["parents"]), args.ref_seconds / n_steps / per_row)))
     gbs_vals = []
-    for i in range(args.warmup + args.steps):
-        gbs, el, sample = oracle_sample(desc, seconds=args.ref_seconds)
+    r0 = 0
+    for i in range(n_steps):
+        el, done = oracle_rows(desc, wl, lib, r0, rows)
+        r0 += rows
         if i >= args.warmup:
-            per_step.append(el)
-            gbs_vals.append(gbs)
+            gbs_vals.append(done / max(el, 1e-9) / 1e9)
     value = statistics.median(gbs_vals)
+    sample = (f"{n_steps} steps of {rows} weight rows per parent of workload '{desc['name']}' at T in "
+              f"{desc['T']} (wide T on 8 columns, scaled by (T+1)/9), about {args.ref_seconds:.0f} s in all")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_bytes(desc) / (value * 1e9),
@@ -505,7 +538,8 @@ def main():
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-seconds", type=float, default=6.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="total host time of the reference arm, split over its steps")
     args = ap.parse_args()
     desc = describe(args.workload)
     if args.impl == "reference":

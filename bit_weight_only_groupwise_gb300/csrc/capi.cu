@@ -226,6 +226,7 @@ qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue,
     if (epilogue != QGEMM_EPILOGUE_STORE && epilogue != QGEMM_EPILOGUE_ADD && epilogue != QGEMM_EPILOGUE_SWIGLU)
         return QGEMM_ERR_INVALID_ARG;
     if (out != QGEMM_OUT_F32 && out != QGEMM_OUT_BF16) return QGEMM_ERR_INVALID_ARG;
+    if (epilogue == QGEMM_EPILOGUE_SWIGLU && plan->N > (1 << 29)) return QGEMM_ERR_SHAPE;   // pair rows fit an int
     plan->epi = epilogue;
     plan->out = out;
     plan->rows = epilogue == QGEMM_EPILOGUE_SWIGLU ? pair_rows(plan->N) : plan->N;

@@ -195,7 +195,8 @@ qgemm_status qgemm_pack_pair(qgemm_codec codec, int F, int K,
  * is F (the output width) and the weights must come from qgemm_pack_pair.
  * The fused outputs run through qgemm_run_ex on one matrix (qgemm_run and
  * qgemm_run_multi take plain STORE / F32 plans only).  Returns
- * QGEMM_ERR_INVALID_ARG for an unknown epilogue or output type, or a bound plan.
+ * QGEMM_ERR_INVALID_ARG for an unknown epilogue or output type, or a bound plan,
+ * and QGEMM_ERR_SHAPE for a SwiGLU plan with F > 2^29.
  */
 qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue, qgemm_out out);
 

@@ -218,6 +218,27 @@ __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t
             if (gate && t < T) store_y(P.Y, P.ybf16, (size_t)t * P.ncols + f, silu_mul(acc[j].x, ux));
             if (gate && t + 1 < T) store_y(P.Y, P.ybf16, (size_t)(t + 1) * P.ncols + f, silu_mul(acc[j].y, uy));
         }
+    } else if (n < P.N && P.epi == EPI_ADD) {
+        // the residual's 64 values in batches of 8 loads before their stores:
+        // one at a time, each add waited a full memory round trip (R may be Y,
+        // so the compiler cannot move a load above an earlier store; every
+        // element is read before it is written either way)
+#pragma unroll
+        for (int jb = 0; jb < 32; jb += 4) {
+            float rv[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = t0 + 2 * (jb + j);
+                rv[2 * j] = t < T ? P.R[(size_t)t * P.ncols + n] : 0.f;
+                rv[2 * j + 1] = t + 1 < T ? P.R[(size_t)(t + 1) * P.ncols + n] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = t0 + 2 * (jb + j);
+                if (t < T) store_y(P.Y, P.ybf16, (size_t)t * P.ncols + n, rv[2 * j] + acc[jb + j].x);
+                if (t + 1 < T) store_y(P.Y, P.ybf16, (size_t)(t + 1) * P.ncols + n, rv[2 * j + 1] + acc[jb + j].y);
+            }
+        }
     } else if (n < P.N) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {

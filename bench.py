@@ -1,17 +1,28 @@
 """Benchmark of the groupwise int4/int5 dequant-GEMM on GB300.
 
-Default workload (N=1): decode/verify widths of the o_proj-shaped int4 matrix,
-N=5120 rows, K=6144, T in {1, 2, 4, 8}.  One step = one call at each of the
-four widths, each on a different copy of the packed weights (24 copies,
-401 MB, rotate so every call streams cold weights from HBM -- the regime the
-"ninfer-3080 docs/performance.md" route boundaries section calls production).
+Default workload (N=1): every configuration of the metric, one call at each
+of its token widths per step:
+
+  tiny       int4   256 x 512,   T = 1
+  decode     int4  5120 x 6144,  T = 1, 2, 4, 8   (decode and verify widths)
+  batched    int4 12288 x 5120,  T = 16, 32, 64, 256
+  multi      int4  4096 x 5120 + int5 12288 x 5120 over one shared X, T = 4, 16, 64
+  prefill_a  int4  7168 x 5120,  T = 256, 1024, 4096
+  prefill_b  int4  5120 x 6144,  T = 256, 1024, 4096
+
+Each (configuration, width) runs as a CUDA graph of R back-to-back calls, each
+call on its own copy of the packed weights, so no call finds its weights in L2
+(between two replays of one graph the rest of the step streams far more than
+the 129 MB L2) -- the cold regime the "ninfer-3080 docs/performance.md" route
+boundaries section calls production.
 
 Metric: achieved HBM GB/s = algorithmic bytes (packed weights + bf16
-activations) per step / step time, with the roofline fraction against the
-measured HBM copy bandwidth, and microseconds per call per T.
+activations, every call of the step) / step time, with per-call microseconds,
+GB/s, TFLOP/s and the fraction of each call's roofline, max((W + X) / HBM,
+2NKT / bf16 tensor peak), and the roofline of every kernel.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|batched|multi|prefill_a|prefill_b|tiny]
+                  [--workload all|decode|batched|multi|prefill_a|prefill_b|tiny|...]
 
 Under torchrun (N > 1) every rank runs its own replica (weak scaling; the path
 needs no collective) and rank 0 prints the line with the max time over ranks.
@@ -40,31 +51,42 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "bit_weight_only_groupwise_gb300", "csrc")
 
-WORKLOADS = {
-    # name: (config name in the generator, widths timed per step)
-    "decode": ("decode", [1, 2, 4, 8]),
-    "batched": ("batched", [16, 32, 64, 256]),
-    "multi": ("multi", [4, 16, 64]),
-    "prefill_a": ("prefill_a", [256, 1024, 4096]),
-    "prefill_b": ("prefill_b", [256, 1024, 4096]),
-    "tiny": ("tiny", [1]),
-    "linear_add": ("linear_add", [1, 2, 4, 8]),
-    "swiglu": ("swiglu", [1, 2, 4, 8]),
-    "decode_fp8": ("decode_fp8", [1, 2, 4, 8]),
-    "prefill_fp8": ("prefill_fp8", [256, 1024, 4096]),
+# the widths timed per configuration of the input generator
+WIDTHS = {
+    "tiny": [1],
+    "decode": [1, 2, 4, 8],
+    "batched": [16, 32, 64, 256],
+    "multi": [4, 16, 64],
+    "prefill_a": [256, 1024, 4096],
+    "prefill_b": [256, 1024, 4096],
+    "linear_add": [1, 2, 4, 8],
+    "swiglu": [1, 2, 4, 8],
+    "decode_fp8": [1, 2, 4, 8],
+    "prefill_fp8": [256, 1024, 4096],
 }
+# a workload is a list of configurations; one step is one call at every width of each
+WORKLOADS = {"all": ["tiny", "decode", "batched", "multi", "prefill_a", "prefill_b"]}
+WORKLOADS.update({name: [name] for name in WIDTHS})
 
 
-def describe(name: str) -> dict:
-    cfg = synth.CONFIGS[WORKLOADS[name][0]]
-    parents = [{"N": N, "K": cfg["K"], "codec": "fp8" if b == 8 else f"int{b}"} for N, b in cfg["parents"]]
-    return {"name": name, "K": cfg["K"], "parents": parents, "T": WORKLOADS[name][1],
-            "outliers": cfg["outliers"], "epilogue": cfg.get("epilogue", "store")}
+def codec_name(bits: int) -> str:
+    return "fp8" if bits == 8 else f"int{bits}"
 
 
 def codec_bits(codec: str) -> int:
     return 8 if codec == "fp8" else int(codec[3:])
+
+
+def describe(name: str) -> dict:
+    configs = []
+    for c in WORKLOADS[name]:
+        cfg = synth.CONFIGS[c]
+        configs.append({"config": c, "K": cfg["K"], "T": WIDTHS[c], "outliers": cfg["outliers"],
+                        "epilogue": cfg.get("epilogue", "store"),
+                        "parents": [{"N": N, "K": cfg["K"], "codec": codec_name(b)} for N, b in cfg["parents"]]})
+    return {"name": name, "configs": configs}
 
 
 def weight_bytes(N: int, K: int, bits: int) -> int:
@@ -72,43 +94,66 @@ def weight_bytes(N: int, K: int, bits: int) -> int:
     return N * K * bits // 8 + 2 * N * (K // 64)
 
 
+def call_bytes(cfg, T) -> int:
+    K = cfg["K"]
+    return sum(weight_bytes(p["N"], K, codec_bits(p["codec"])) for p in cfg["parents"]) + 2 * T * K
+
+
+def call_flops(cfg, T) -> int:
+    return sum(2 * T * p["N"] * cfg["K"] for p in cfg["parents"])
+
+
+def calls(desc):
+    """(config index, config, T) of every call of one step."""
+    return [(i, c, T) for i, c in enumerate(desc["configs"]) for T in c["T"]]
+
+
 def step_bytes(desc) -> int:
-    K = desc["K"]
-    total = 0
-    for T in desc["T"]:
-        total += sum(weight_bytes(p["N"], K, codec_bits(p["codec"])) for p in desc["parents"]) + 2 * T * K
-    return total
+    return sum(call_bytes(c, T) for _, c, T in calls(desc))
+
+
+def config_summary(desc) -> dict:
+    return {"workload": desc["name"],
+            "calls": {c["config"]: {"parents": c["parents"], "K": c["K"], "T": c["T"], "epilogue": c["epilogue"]}
+                      for c in desc["configs"]}}
+
+
+def _peak(key, fallback):
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)[key]), "measured"
+    except Exception:
+        return fallback, "fallback"
 
 
 def hbm_peak():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
-    except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+    return _peak("hbm_gbs", FALLBACK_HBM_GBS)
 
 
 def tensor_peak():
     """Dense bf16 tensor throughput (burst: each call is a short kernel)."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            return float(json.load(f)["bf16_tflops"]), "measured"
-    except Exception:
-        return FALLBACK_BF16_TFLOPS, "fallback"
+    return _peak("bf16_tflops", FALLBACK_BF16_TFLOPS)
+
+
+def call_bound(cfg, T, hbm, tens) -> tuple:
+    """(bound, roofline seconds) of one call by the metric's formula."""
+    t_mem = call_bytes(cfg, T) / (hbm * 1e9)
+    t_tc = call_flops(cfg, T) / (tens * 1e12)
+    return ("hbm", t_mem) if t_mem >= t_tc else ("tensor", t_tc)
 
 
 def route_kernel(route: str, K: int) -> tuple:
-    """(kernel name, source file, bound) of the kernel a route launches."""
+    """(kernel name, source file) of the kernel a route launches."""
     if route.startswith("tcgen05"):
-        return "qg::wide_kernel", "wide.cu", "tensor"
+        return "qg::wide_kernel", "wide.cu"
     full = (K // 64) % 8 == 0 and 1 <= (K // 64) // 8 <= 16
-    return ("qg::skinny_line_kernel" if full else "qg::skinny_kernel"), "skinny.cu", "hbm"
+    return ("qg::skinny_line_kernel" if full else "qg::skinny_kernel"), "skinny.cu"
 
 
-def recorded_traffic(kernel_src: str, profile_name: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on this kernel source."""
+def recorded_traffic(kernel_src: str, profile_name: str, keys):
+    """Mean per-launch DRAM bytes over the calls `keys` ("config:T") from a
+    committed ncu summary, if it was taken on this kernel source and covers
+    every one of them; else None."""
     path = os.path.join(PROFILES, profile_name)
     if not os.path.exists(path):
         return None
@@ -121,7 +166,8 @@ def recorded_traffic(kernel_src: str, profile_name: str):
     if rec.get("kernel_source_sha256") != want:
         return None
     try:
-        return json.loads(rec["dram_bytes_per_launch"])
+        by_call = json.loads(rec["dram_bytes_by_call"])
+        return statistics.fmean(by_call[k] for k in keys)
     except Exception:
         return None
 
@@ -205,60 +251,62 @@ def barrier(world: int):
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(desc, seconds: float = 12.0):
-    """Time the fp64 oracle on whole calls of the workload for about `seconds`."""
+def _oracle_call(lib, wl, cfg, T, rows=None, r0=0):
+    """Seconds of the oracle on one call (every parent) at width T, on
+    min(T, 8) columns scaled by (T + 1) / (cols + 1) (the row dequantisation
+    costs about one column; the rest is linear in T by column independence),
+    optionally on `rows` weight rows (cyclic from r0) of each parent; returns
+    (seconds, algorithmic bytes of that share of the call)."""
     import oracle
-    wl = synth.workload(desc["name"] if desc["name"] in synth.CONFIGS else WORKLOADS[desc["name"]][0],
-                        max(desc["T"]))
-    lib = oracle.load()
-    done_bytes, elapsed, calls = 0, 0.0, []
-    K = desc["K"]
-    # narrow widths first; wide ones on a column subset (cost is linear in T)
-    while elapsed < seconds:
-        for T in desc["T"]:
-            cols = min(T, 8)
-            x = wl["x"][:cols]
-            t0 = time.perf_counter()
-            for p in wl["parents"]:
-                oracle.gemm_parent(p, x, lib=lib)
-            dt = time.perf_counter() - t0
-            # the row dequantisation costs about one column's dot products
-            scale = (T + 1) / (cols + 1)
-            elapsed += dt * scale
-            calls.append((T, cols))
-            done_bytes += sum(weight_bytes(p["N"], K, p["bits"]) for p in wl["parents"]) + 2 * T * K
-            if elapsed >= seconds:
-                break
-    extrap = any(T != c for T, c in calls)
-    sample = (f"{len(calls)} oracle calls of workload '{desc['name']}' at T in {desc['T']}"
-              + ("; wide T timed on 8 columns and scaled by (T+1)/9 (cost is linear in T)" if extrap else ""))
-    return done_bytes / elapsed / 1e9, elapsed, sample
-
-
-def oracle_rows(desc, wl, lib, r0: int, nrows: int):
-    """Time the oracle on rows [r0, r0 + nrows) (cyclic) of every parent at
-    every width of the step; returns (seconds, algorithmic bytes of that share
-    of the step).  Wide widths run on 8 columns and scale by (T+1)/9."""
-    import oracle
-    K = desc["K"]
+    K = cfg["K"]
+    cols = min(T, 8)
+    x = wl["x"][:cols]
     elapsed, done = 0.0, 0.0
-    for T in desc["T"]:
-        cols = min(T, 8)
-        x = wl["x"][:cols]
-        for p in wl["parents"]:
-            N = p["N"]
-            n = min(nrows, N)
+    for p in wl["parents"]:
+        N = p["N"]
+        if rows is None:
+            t0 = time.perf_counter()
+            oracle.gemm_parent(p, x, lib=lib)
+            dt = time.perf_counter() - t0
+            n = N
+        else:
+            n = min(rows, N)
             idx = (r0 + np.arange(n)) % N
             t0 = time.perf_counter()
             oracle.gemm(p["bits"], p["packed"][idx], p["scales"][idx], x, n, K, lib=lib)
-            elapsed += (time.perf_counter() - t0) * (T + 1) / (cols + 1)
-            done += weight_bytes(n, K, p["bits"]) + 2 * T * K * n / N
+            dt = time.perf_counter() - t0
+        elapsed += dt * (T + 1) / (cols + 1)
+        done += weight_bytes(n, K, p["bits"]) + 2 * T * K * n / N
     return elapsed, done
+
+
+def _oracle_inputs(desc):
+    # the oracle runs on at most 8 columns (activations are prefix-consistent)
+    return [synth.workload(c["config"], min(8, max(c["T"]))) for c in desc["configs"]]
+
+
+def oracle_sample(desc, seconds: float = 12.0):
+    """Time the fp64 oracle on whole calls of the workload for about `seconds`."""
+    import oracle
+    lib = oracle.load()
+    wls = _oracle_inputs(desc)
+    done_bytes, elapsed, n = 0.0, 0.0, 0
+    while elapsed < seconds:
+        for ci, c, T in calls(desc):
+            dt, b = _oracle_call(lib, wls[ci], c, T)
+            elapsed += dt
+            done_bytes += b
+            n += 1
+            if elapsed >= seconds:
+                break
+    sample = (f"{n} oracle calls of workload '{desc['name']}' in step order (every parent, whole weight "
+              f"matrices); widths above 8 timed on 8 columns and scaled by (T+1)/9 (cost is linear in T)")
+    return done_bytes / elapsed / 1e9, elapsed, sample
 
 
 def run_reference(args, desc):
     """The fp64 oracle on the host cores, as it stands: each step times it on
-    a slice of the weight rows (every parent, every width), sized so that the
+    a slice of the weight rows of every call of the step, sized so that the
     whole --warmup + --steps run takes about --ref-seconds; the value is the
     median over the timed steps of the slice's algorithmic bytes per second."""
     world, rank, _ = dist_env()
@@ -266,27 +314,37 @@ def run_reference(args, desc):
         return 0
     import oracle
     lib = oracle.load()
-    wl = synth.workload(WORKLOADS[desc["name"]][0], max(desc["T"]))
+    wls = _oracle_inputs(desc)
     n_steps = args.warmup + args.steps
+
+    def step(rows, r0):
+        el, done = 0.0, 0.0
+        for ci, c, T in calls(desc):
+            dt, b = _oracle_call(lib, wls[ci], c, T, rows=rows, r0=r0)
+            el += dt
+            done += b
+        return el, done
+
     # calibrate: seconds per weight row of a step
-    t_cal, _ = oracle_rows(desc, wl, lib, 0, 32)
-    per_row = max(t_cal / 32, 1e-7)
-    rows = int(max(1, min(max(p["N"] for p in wl["parents"]), args.ref_seconds / n_steps / per_row)))
+    t_cal, _ = step(16, 0)
+    per_row = max(t_cal / 16, 1e-7)
+    max_rows = max(p["N"] for c in desc["configs"] for p in c["parents"])
+    rows = int(max(1, min(max_rows, args.ref_seconds / n_steps / per_row)))
     gbs_vals = []
     r0 = 0
     for i in range(n_steps):
-        el, done = oracle_rows(desc, wl, lib, r0, rows)
+        el, done = step(rows, r0)
         r0 += rows
         if i >= args.warmup:
             gbs_vals.append(done / max(el, 1e-9) / 1e9)
     value = statistics.median(gbs_vals)
-    sample = (f"{n_steps} steps of {rows} weight rows per parent of workload '{desc['name']}' at T in "
-              f"{desc['T']} (wide T on 8 columns, scaled by (T+1)/9), about {args.ref_seconds:.0f} s in all")
+    sample = (f"{n_steps} steps of {rows} weight rows per parent of every call of workload '{desc['name']}' "
+              f"(widths above 8 on 8 columns, scaled by (T+1)/9), about {args.ref_seconds:.0f} s in all")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_bytes(desc) / (value * 1e9),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc["name"], "parents": desc["parents"], "K": desc["K"], "T": desc["T"]},
+        "config": config_summary(desc),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -295,6 +353,78 @@ def run_reference(args, desc):
 
 
 # ---------------------------------------------------------------- GPU arm
+
+class Config:
+    """One configuration's weights (R packed copies, one plan each), inputs and outputs."""
+
+    def __init__(self, qg, torch, dev, cfg, copies, pdl):
+        self.cfg = cfg
+        K = cfg["K"]
+        Ts = cfg["T"]
+        T_max = max(Ts)
+        wl = synth.workload(cfg["config"], T_max, seed=0)
+        self.wl = wl
+        parents = wl["parents"]
+        self.epi = cfg["epilogue"]
+        epi_code = {"store": qg.QGEMM_EPILOGUE_STORE, "add": qg.QGEMM_EPILOGUE_ADD,
+                    "swiglu": qg.QGEMM_EPILOGUE_SWIGLU}[self.epi]
+        if self.epi == "swiglu":
+            # the gate/up pair (parents 0 and 1) packed as one matrix with one output
+            g, u = parents
+            base = [qg.SwiGLUPair(g["bits"], g["N"], K, g["packed"], g["scales"], u["packed"], u["scales"], T_max)]
+            self.set_bytes = qg.qgemm_pair_packed_bytes(g["N"], K, g["bits"])
+            self.out_cols = [g["N"]]
+        else:
+            base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max, epilogue=epi_code)
+                    for p in parents]
+            self.set_bytes = sum(qg.qgemm_packed_bytes(p["N"], K, p["bits"]) for p in parents)
+            self.out_cols = [p["N"] for p in parents]
+        self.sets = []
+        for i in range(copies):
+            ws = []
+            for b in base:
+                w = type(b).__new__(type(b))
+                w.codec, w.N, w.K, w.T_max, w.epilogue, w.out = b.codec, b.N, b.K, b.T_max, b.epilogue, b.out
+                w.device = dev
+                w.packed = b.packed.clone() if i else b.packed
+                st, w.plan = qg.qgemm_plan(b.N, K, b.codec, T_max)
+                qg.check(st, "qgemm_plan")
+                if self.epi != "store":
+                    qg.check(qg.qgemm_plan_set_epilogue(w.plan, epi_code, qg.QGEMM_OUT_F32), "set_epilogue")
+                wsb = qg.qgemm_plan_workspace_bytes(w.plan)
+                w.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+                qg.check(qg.qgemm_plan_bind(w.plan, w.packed, w.workspace, w.workspace.numel()), "bind")
+                qg.check(qg.qgemm_plan_set_pdl(w.plan, pdl), "set_pdl")
+                ws.append(w)
+            self.sets.append(ws)
+        self.xs = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).to(dev) for T in Ts}
+        self.ys = {T: [torch.empty((T, n), dtype=torch.float32, device=dev) for n in self.out_cols] for T in Ts}
+        # the residual of a LinearAdd: fp32 [T, N], seeded
+        self.rs = {T: torch.from_numpy(np.random.default_rng(T).normal(0, 8, (T, self.out_cols[0]))
+                                       .astype(np.float32)).to(dev) for T in Ts} if self.epi == "add" else {}
+
+    def call(self, qg, torch, i, T, X=None, Ys=None, Rt=None):
+        ws = self.sets[i % len(self.sets)]
+        X = self.xs[T] if X is None else X
+        Ys = self.ys[T] if Ys is None else Ys
+        s = torch.cuda.current_stream()
+        if self.epi != "store":
+            Rt = (self.rs[T] if Rt is None else Rt) if self.epi == "add" else None
+            st = qg.qgemm_run_ex(ws[0].plan, X, T, Rt, Ys[0], s)
+        elif len(ws) == 1:
+            st = qg.qgemm_run(ws[0].plan, X, T, Ys[0], s)
+        else:
+            st = qg.qgemm_run_multi([w.plan for w in ws], X, T, Ys, s)
+        if st != qg.QGEMM_OK:
+            raise qg.QgemmError(st, "run")
+
+    def launches(self, T) -> int:
+        """Kernels one call at width T launches (the tcgen05 route runs one
+        launch per codec among a call's parents)."""
+        if self.sets[0][0].route(T).startswith("tcgen05"):
+            return len({w.codec for w in self.sets[0]})
+        return 1
+
 
 def run_ours(args, desc):
     import torch
@@ -307,92 +437,47 @@ def run_ours(args, desc):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-    K = desc["K"]
-    Ts = desc["T"]
-    T_max = max(Ts)
 
-    # weights: each parent packed once, then copied so that the rotation exceeds 3x L2
-    wl = synth.workload(WORKLOADS[desc["name"]][0], T_max, seed=0)
-    parents = wl["parents"]
-    epi = desc["epilogue"]
-    epi_code = {"store": qg.QGEMM_EPILOGUE_STORE, "add": qg.QGEMM_EPILOGUE_ADD,
-                "swiglu": qg.QGEMM_EPILOGUE_SWIGLU}[epi]
-    if epi == "swiglu":
-        # the gate/up pair (parents 0 and 1) packed as one matrix with one output
-        g, u = parents
-        base = [qg.SwiGLUPair(g["bits"], g["N"], K, g["packed"], g["scales"], u["packed"], u["scales"], T_max)]
-        set_bytes = qg.qgemm_pair_packed_bytes(g["N"], K, g["bits"])
-        out_cols = [g["N"]]
-    else:
-        base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max, epilogue=epi_code)
-                for p in parents]
-        set_bytes = sum(qg.qgemm_packed_bytes(p["N"], K, p["bits"]) for p in parents)
-        out_cols = [p["N"] for p in parents]
-    copies = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)))
-    weight_sets = []
-    for i in range(copies):
-        ws = []
-        for b in base:
-            w = type(b).__new__(type(b))
-            w.codec, w.N, w.K, w.T_max, w.epilogue, w.out = b.codec, b.N, b.K, b.T_max, b.epilogue, b.out
-            w.packed = b.packed.clone() if i else b.packed
-            st, w.plan = qg.qgemm_plan(b.N, K, b.codec, T_max)
-            qg.check(st, "qgemm_plan")
-            if epi != "store":
-                qg.check(qg.qgemm_plan_set_epilogue(w.plan, epi_code, qg.QGEMM_OUT_F32), "set_epilogue")
-            wsb = qg.qgemm_plan_workspace_bytes(w.plan)
-            w.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
-            qg.check(qg.qgemm_plan_bind(w.plan, w.packed, w.workspace, w.workspace.numel()), "bind")
-            qg.check(qg.qgemm_plan_set_pdl(w.plan, not args.no_pdl), "set_pdl")
-            ws.append(w)
-        weight_sets.append(ws)
-    xs = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).to(dev) for T in Ts}
-    ys = {T: [torch.empty((T, n), dtype=torch.float32, device=dev) for n in out_cols] for T in Ts}
-    # the residual of a LinearAdd: fp32 [T, N], seeded
-    rs = {T: torch.from_numpy(np.random.default_rng(T).normal(0, 8, (T, out_cols[0])).astype(np.float32)).to(dev)
-          for T in Ts} if epi == "add" else {}
+    # R calls per graph, each on its own packed copy; a single small
+    # configuration rotates enough copies to exceed 3x L2 on its own
+    R = max(d for d in range(1, min(args.calls_per_graph, args.steps) + 1) if args.steps % d == 0)
+    blocks = args.steps // R
+    cfgs = []
+    for c in desc["configs"]:
+        set_bytes = sum(qg.qgemm_packed_bytes(p["N"], c["K"], codec_bits(p["codec"])) for p in c["parents"])
+        copies = R if len(desc["configs"]) > 1 else max(R, min(256, int(np.ceil(3 * L2_BYTES / set_bytes))))
+        cfgs.append(Config(qg, torch, dev, c, copies, not args.no_pdl))
     torch.cuda.synchronize()
 
-    def call(ws, T, X=None, Ys=None, Rt=None):
-        X = xs[T] if X is None else X
-        Ys = ys[T] if Ys is None else Ys
-        if epi != "store":
-            Rt = (rs[T] if Rt is None else Rt) if epi == "add" else None
-            st = qg.qgemm_run_ex(ws[0].plan, X, T, Rt, Ys[0], torch.cuda.current_stream())
-        elif len(ws) == 1:
-            st = qg.qgemm_run(ws[0].plan, X, T, Ys[0], torch.cuda.current_stream())
-        else:
-            st = qg.qgemm_run_multi([w.plan for w in ws], X, T, Ys, torch.cuda.current_stream())
-        if st != qg.QGEMM_OK:
-            raise qg.QgemmError(st, "run")
-
-    # eager warm-up (loads the kernels), then one CUDA graph per (T, chunk of the
-    # copy rotation) holding R calls, so that host launch cost stays off the clock
-    for T in Ts:
-        for ws in weight_sets[:2]:
-            call(ws, T)
+    # eager warm-up (loads the kernels), then one CUDA graph per (call, chunk
+    # of the copy rotation) holding R calls, so that host launch cost stays
+    # off the clock
+    for ci, c, T in calls(desc):
+        for i in range(2):
+            cfgs[ci].call(qg, torch, i, T)
     torch.cuda.synchronize()
     assert qg.qgemm_device_status(stream) == qg.QGEMM_OK
-    R = max(d for d in range(1, min(copies, args.steps) + 1) if args.steps % d == 0)
-    n_chunks = (copies + R - 1) // R
     graphs = {}
     cap_stream = torch.cuda.Stream()
-    for T in Ts:
-        graphs[T] = []
-        for ci in range(n_chunks):
+    for ci, c, T in calls(desc):
+        n_chunks = (len(cfgs[ci].sets) + R - 1) // R
+        gl = []
+        for ch in range(n_chunks):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap_stream):
                 for r in range(R):
-                    call(weight_sets[(ci * R + r) % copies], T)
-            graphs[T].append(g)
+                    cfgs[ci].call(qg, torch, ch * R + r, T)
+            gl.append(g)
+        graphs[(ci, T)] = gl
     torch.cuda.synchronize()
-    blocks = args.steps // R
+    keys = [(ci, T) for ci, _, T in calls(desc)]
 
     def replay_block(b, evs=None):
-        for j, T in enumerate(Ts):
+        for j, k in enumerate(keys):
             if evs is not None:
                 evs[j][0].record(stream)
-            graphs[T][b % n_chunks].replay()
+            gl = graphs[k]
+            gl[b % len(gl)].replay()
             if evs is not None:
                 evs[j][1].record(stream)
 
@@ -401,12 +486,11 @@ def run_ours(args, desc):
             replay_block(b)
     torch.cuda.synchronize()
 
-    # timed region: exactly K steps = K/R replays of every width's R-call graph;
-    # events around each replay on the launching stream give per-T call times
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in Ts]
+    # timed region: exactly K steps = K/R replays of every call's R-call graph;
+    # events around each replay on the launching stream give per-call times
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in keys]
           for _ in range(blocks)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_launch0 = qg.qgemm_launch_count()
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clocks:
@@ -417,85 +501,101 @@ def run_ours(args, desc):
             stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    # graph replays do not pass through the host entry points: count the
-    # kernels the replayed graphs hold: one per call, except that the tcgen05
-    # route launches once per codec among the parents
-    n_codecs = len({p["codec"] for p in desc["parents"]})
-    launches = blocks * R * sum(n_codecs if weight_sets[0][0].route(T).startswith("tcgen05") else 1 for T in Ts)
     elapsed_ms = max_over_ranks(start.elapsed_time(stop), world)
-    per_T_ms = {T: [ev[b][j][0].elapsed_time(ev[b][j][1]) / R for b in range(blocks)] for j, T in enumerate(Ts)}
+    per_call_ms = {k: [ev[b][j][0].elapsed_time(ev[b][j][1]) / R for b in range(blocks)] for j, k in enumerate(keys)}
     assert qg.qgemm_device_status(stream) == qg.QGEMM_OK
-    del n_launch0
+    # graph replays do not pass through the host entry points: the kernels the
+    # replayed graphs hold
+    launches = blocks * R * sum(cfgs[ci].launches(T) for ci, T in keys)
 
     sb = step_bytes(desc)
     value = world * args.steps * sb / (elapsed_ms * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
-    per_T = {}
-    by_kernel = {}          # kernel -> [time ms, bytes, flops, launches] over the timed region
-    for T in Ts:
-        b = sum(weight_bytes(p["N"], K, codec_bits(p["codec"])) for p in desc["parents"]) + 2 * T * K
-        flops = sum(2 * T * p["N"] * K for p in desc["parents"])
-        med = statistics.median(per_T_ms[T])
-        mean = statistics.fmean(per_T_ms[T])
-        route = ",".join(w.route(T) for w in weight_sets[0])
-        per_T[str(T)] = {"us_per_call": 1e3 * med, "gbs": b / (med * 1e-3) / 1e9,
-                         "frac": b / (med * 1e-3) / 1e9 / peak,
-                         "tflops": flops / (med * 1e-3) / 1e12, "route": route}
-        kern = route_kernel(weight_sets[0][0].route(T), K)
-        acc = by_kernel.setdefault(kern, [0.0, 0, 0, 0])
+    hbm, hbm_kind = hbm_peak()
+    tens, tens_kind = tensor_peak()
+    per_call = {}
+    groups = {}         # (kernel, bound) -> [time ms, bytes, flops, launches, call keys]
+    for ci, c, T in calls(desc):
+        k = (ci, T)
+        b = call_bytes(c, T)
+        fl = call_flops(c, T)
+        med = statistics.median(per_call_ms[k])
+        mean = statistics.fmean(per_call_ms[k])
+        route = ",".join(w.route(T) for w in cfgs[ci].sets[0])
+        bound, t_roof = call_bound(c, T, hbm, tens)
+        name = f"{c['config']}:{T}"
+        per_call[name] = {"us_per_call": 1e3 * med, "gbs": b / (med * 1e-3) / 1e9, "hbm_frac": b / (med * 1e-3) / 1e9 / hbm,
+                          "tflops": fl / (med * 1e-3) / 1e12, "tensor_frac": fl / (med * 1e-3) / 1e12 / tens,
+                          "bound": bound, "roofline_us": 1e6 * t_roof, "frac": 1e6 * t_roof / (1e3 * med),
+                          "columns_per_s": T / (med * 1e-3), "route": route}
+        kname, ksrc = route_kernel(cfgs[ci].sets[0][0].route(T), c["K"])
+        acc = groups.setdefault((kname, ksrc, bound), [0.0, 0, 0, 0, []])
+        n = blocks * R * cfgs[ci].launches(T)
         acc[0] += mean * blocks * R
         acc[1] += b * blocks * R
-        acc[2] += flops * blocks * R
-        acc[3] += blocks * R
-    # the roofline of the kernel that takes most of the timed region: HBM bytes
-    # for the weight-streaming kernels, tensor FLOPs for the tcgen05 route
-    (kname, ksrc, bound), (k_ms, k_bytes, k_flops, k_launches) = max(by_kernel.items(), key=lambda kv: kv[1][0])
-    profile_stem = kname.split("::")[-1]
-    traffic = recorded_traffic(os.path.join(ROOT, "bit_weight_only_groupwise_gb300", "csrc", ksrc),
-                               f"{profile_stem}_{desc['name']}_traffic.md")
-    if bound == "hbm":
-        achieved = k_bytes / (k_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_source": peak_kind, "kernel": kname,
-                "algorithmic_bytes_per_launch": k_bytes / k_launches}
-    else:
-        tpeak, tkind = tensor_peak()
-        achieved = k_flops / (k_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": achieved / tpeak, "traffic": traffic, "peak_source": tkind, "kernel": kname,
-                "algorithmic_flops_per_launch": k_flops / k_launches}
+        acc[2] += fl * blocks * R
+        acc[3] += n
+        acc[4].append(name)
 
-    # end to end: pinned host X -> device, the call, device Y -> pinned host, every step
+    def roofline(kname, ksrc, bound, g):
+        k_ms, k_bytes, k_flops, k_launches, names = g
+        traffic = recorded_traffic(os.path.join(CSRC, ksrc), f"{kname.split('::')[-1]}_{desc['name']}_traffic.md",
+                                   names)
+        if bound == "hbm":
+            achieved = k_bytes / (k_ms * 1e-3) / 1e9
+            return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": traffic, "peak_source": hbm_kind, "kernel": kname, "calls": names,
+                    "algorithmic_bytes_per_launch": k_bytes / k_launches, "share_of_step": 0.0}
+        achieved = k_flops / (k_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": tens, "unit": "TFLOP/s", "frac": achieved / tens,
+                "traffic": traffic, "peak_source": tens_kind, "kernel": kname, "calls": names,
+                "algorithmic_flops_per_launch": k_flops / k_launches, "share_of_step": 0.0}
+
+    total_ms = sum(g[0] for g in groups.values())
+    rooflines = []
+    for (kname, ksrc, bound), g in sorted(groups.items(), key=lambda kv: -kv[1][0]):
+        r = roofline(kname, ksrc, bound, g)
+        r["share_of_step"] = g[0] / total_ms
+        rooflines.append(r)
+    # the roofline of the kernel (and bound) taking most of the timed region
+    roof = rooflines[0]
+
+    # end to end: pinned host X -> device, the call, device Y -> pinned host,
+    # for every call of the step
     e2e = None
     if not args.no_e2e:
-        hx = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).pin_memory() for T in Ts}
-        hy = {T: [torch.empty((T, n), dtype=torch.float32).pin_memory() for n in out_cols] for T in Ts}
-        dx = {T: torch.empty_like(xs[T]) for T in Ts}
-        hr = {T: rs[T].cpu().pin_memory() for T in rs}
-        dr = {T: torch.empty_like(rs[T]) for T in rs}
-        h2d = sum(hx[T].numel() * 2 for T in Ts) + sum(hr[T].numel() * 4 for T in hr)
-        d2h = sum(y.numel() * 4 for T in Ts for y in hy[T])
-        e_steps = max(1, min(args.steps, 2000))
+        hx, hy, dx, hr, dr = {}, {}, {}, {}, {}
+        for ci, c, T in calls(desc):
+            cf = cfgs[ci]
+            hx[(ci, T)] = torch.from_numpy(cf.wl["x"][:T].view(np.int16).copy()).pin_memory()
+            hy[(ci, T)] = [torch.empty((T, n), dtype=torch.float32).pin_memory() for n in cf.out_cols]
+            dx[(ci, T)] = torch.empty_like(cf.xs[T])
+            if cf.epi == "add":
+                hr[(ci, T)] = cf.rs[T].cpu().pin_memory()
+                dr[(ci, T)] = torch.empty_like(cf.rs[T])
+        h2d = sum(h.numel() * 2 for h in hx.values()) + sum(h.numel() * 4 for h in hr.values())
+        d2h = sum(y.numel() * 4 for ys in hy.values() for y in ys)
+        e_steps = max(1, min(args.steps, args.e2e_steps))
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(e_steps):
-            for T in Ts:
-                dx[T].copy_(hx[T], non_blocking=True)
-                if epi == "add":
-                    dr[T].copy_(hr[T], non_blocking=True)
-                call(weight_sets[i % copies], T, X=dx[T], Rt=dr.get(T))
-                for y, h in zip(ys[T], hy[T]):
+            for ci, c, T in calls(desc):
+                k = (ci, T)
+                dx[k].copy_(hx[k], non_blocking=True)
+                if k in hr:
+                    dr[k].copy_(hr[k], non_blocking=True)
+                cfgs[ci].call(qg, torch, i, T, X=dx[k], Rt=dr.get(k))
+                for y, h in zip(cfgs[ci].ys[T], hy[k]):
                     h.copy_(y, non_blocking=True)
             stream.synchronize()          # the step's results are on the host
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(max(e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0)), world)
         e2e = {"value": world * e_steps * sb / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / e_steps,
+               "steps": e_steps}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -504,17 +604,24 @@ def run_ours(args, desc):
                "seconds": el, "host_cores": os.cpu_count()}
 
     if rank == 0:
+        l2 = (f"each call of a graph streams its own packed copy ({R} copies per configuration); between two "
+              f"replays of a graph the rest of the step streams more than 3x the L2")
+        if len(desc["configs"]) == 1:
+            cf = cfgs[0]
+            rot = len(cf.sets) * cf.set_bytes
+            l2 = (f"rotating {len(cf.sets)} packed-weight copies ({rot / 1e6:.0f} MB"
+                  + (" > 3x L2)" if rot > 3 * L2_BYTES else ", warm: less than 3x L2)"))
+        config = config_summary(desc)
+        config.update({"l2": l2, "parallelism": "replicas" if world > 1 else "single", "pdl": not args.no_pdl,
+                       "calls_per_graph": R})
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": desc["name"], "parents": desc["parents"], "K": desc["K"], "T": Ts,
-                       "epilogue": epi,
-                       "l2": f"rotating {copies} packed-weight copies ({copies * set_bytes / 1e6:.0f} MB > 3x L2)",
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "pdl": not args.no_pdl},
-            "per_T": per_T,
+            "config": config,
+            "per_call": per_call,
             "roofline": roof,
+            "rooflines": rooflines,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -530,11 +637,14 @@ def run_ours(args, desc):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=48000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="all")
+    ap.add_argument("--calls-per-graph", type=int, default=10,
+                    help="R: calls of one (configuration, width) per CUDA graph (a divisor of --steps)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

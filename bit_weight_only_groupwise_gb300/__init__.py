@@ -46,7 +46,7 @@ EXPORTS = [
     "qgemm_plan_workspace_bytes", "qgemm_plan_bind", "qgemm_run", "qgemm_run_multi",
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
     "qgemm_device_status", "qgemm_plan_set_pdl", "qgemm_pair_packed_bytes", "qgemm_pack_pair",
-    "qgemm_plan_set_epilogue", "qgemm_run_ex", "qgemm_selftest_timeout",
+    "qgemm_plan_set_epilogue", "qgemm_run_ex", "qgemm_selftest_timeout", "qgemm_plan_force_route",
 ]
 
 _lock = threading.Lock()
@@ -82,6 +82,7 @@ def _declare(lib):
         "qgemm_plan_set_epilogue": ([vp, i32, i32], i32),
         "qgemm_run_ex": ([vp, vp, i32, vp, vp, vp], i32),
         "qgemm_selftest_timeout": ([vp], i32),
+        "qgemm_plan_force_route": ([vp, i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -195,6 +196,10 @@ def qgemm_plan_route(plan, T: int) -> int:
     return load().qgemm_plan_route(plan, T)
 
 
+def qgemm_plan_force_route(plan, route: int) -> int:
+    return load().qgemm_plan_force_route(plan, route)
+
+
 def qgemm_route_name(route: int) -> str:
     return load().qgemm_route_name(route).decode()
 
@@ -217,6 +222,38 @@ def check(status: int, what: str = "") -> None:
 
 
 # ------------------------------------------------------------ convenience holders
+
+def _check_tensor(t, shape, dtypes, device, what):
+    """Raise QgemmError(QGEMM_ERR_SHAPE) unless t is a contiguous tensor of
+    the given shape and one of the given dtypes on the given device.  The C
+    entry points see only pointers, so a wrong extent here would make a
+    kernel read or write past a buffer."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise QgemmError(QGEMM_ERR_INVALID_ARG, f"{what}: expected a torch tensor, got {type(t).__name__}")
+    if t.dtype not in dtypes:
+        raise QgemmError(QGEMM_ERR_SHAPE, f"{what}: dtype {t.dtype}, expected one of {list(dtypes)}")
+    if tuple(t.shape) != tuple(shape):
+        raise QgemmError(QGEMM_ERR_SHAPE, f"{what}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise QgemmError(QGEMM_ERR_SHAPE, f"{what}: not contiguous")
+    if t.device != device:
+        raise QgemmError(QGEMM_ERR_INVALID_ARG, f"{what}: on {t.device}, expected {device}")
+
+
+def _x_dtypes():
+    import torch
+    # bf16 values, or their bit patterns in a 16-bit integer tensor
+    return (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+def _check_x(X, K, device):
+    import torch
+    if not isinstance(X, torch.Tensor) or X.dim() != 2:
+        raise QgemmError(QGEMM_ERR_SHAPE, "X: expected a 2-D tensor [T, K]")
+    _check_tensor(X, (X.shape[0], K), _x_dtypes(), device, "X")
+    return X.shape[0]
+
 
 def _to_dev(a, dtype, dev):
     import numpy as np
@@ -243,6 +280,9 @@ class GroupwiseWeights:
         self.codec, self.N, self.K, self.T_max = codec, N, K, T_max
         self.epilogue, self.out = epilogue, out
         dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         codes = _to_dev(codes_canonical, np.uint8, dev)
         scales = _to_dev(scales_fp16, np.int16, dev)
         nbytes = qgemm_packed_bytes(N, K, codec)
@@ -267,12 +307,20 @@ class GroupwiseWeights:
 
     def run(self, X, Y=None, stream=None, R=None):
         """Y = epilogue(X[T, K] (bf16) . deq(W)^T): fp32 or bf16 [T, N] ([T, F]
-        for a SwiGLU pair); R is the fp32 [T, N] residual of an ADD plan."""
+        for a SwiGLU pair); R is the fp32 [T, N] residual of an ADD plan.
+
+        X, Y and R must be contiguous tensors of exactly these shapes and
+        dtypes on the weights' device (X may hold bf16 bit patterns as int16);
+        anything else raises QgemmError before any launch."""
         import torch
-        T = X.shape[0]
+        T = _check_x(X, self.K, self.device)
+        ydtype = torch.bfloat16 if self.out == QGEMM_OUT_BF16 else torch.float32
         if Y is None:
-            dtype = torch.bfloat16 if self.out == QGEMM_OUT_BF16 else torch.float32
-            Y = torch.empty((T, self.N), dtype=dtype, device=X.device)
+            Y = torch.empty((T, self.N), dtype=ydtype, device=X.device)
+        else:
+            _check_tensor(Y, (T, self.N), (ydtype,), self.device, "Y")
+        if R is not None:
+            _check_tensor(R, (T, self.N), (torch.float32,), self.device, "R")
         if (self.epilogue, self.out) == (QGEMM_EPILOGUE_STORE, QGEMM_OUT_F32) and R is None:
             check(qgemm_run(self.plan, X, T, Y, stream), "qgemm_run")
         else:
@@ -292,11 +340,27 @@ class GroupwiseWeights:
 
 
 def run_multi(weights, X, Ys=None, stream=None):
-    """Several GroupwiseWeights (same K) over one shared X in one launch."""
+    """Several GroupwiseWeights (same K) over one shared X in one launch.
+
+    X and every Ys[i] are checked as in GroupwiseWeights.run (X [T, K]
+    bf16, Ys[i] fp32 [T, N_i], contiguous, on the weights' device)."""
     import torch
-    T = X.shape[0]
+    if not weights:
+        raise QgemmError(QGEMM_ERR_INVALID_ARG, "run_multi: no weights")
+    dev = weights[0].device
+    for w in weights:
+        if w.K != weights[0].K:
+            raise QgemmError(QGEMM_ERR_SHAPE, "run_multi: parents differ in K")
+        if w.device != dev:
+            raise QgemmError(QGEMM_ERR_INVALID_ARG, "run_multi: parents on different devices")
+    T = _check_x(X, weights[0].K, dev)
     if Ys is None:
         Ys = [torch.empty((T, w.N), dtype=torch.float32, device=X.device) for w in weights]
+    else:
+        if len(Ys) != len(weights):
+            raise QgemmError(QGEMM_ERR_INVALID_ARG, "run_multi: one output per parent")
+        for i, (w, y) in enumerate(zip(weights, Ys)):
+            _check_tensor(y, (T, w.N), (torch.float32,), dev, f"Ys[{i}]")
     check(qgemm_run_multi([w.plan for w in weights], X, T, Ys, stream), "qgemm_run_multi")
     return Ys
 
@@ -312,6 +376,9 @@ class SwiGLUPair(GroupwiseWeights):
         self.codec, self.N, self.K, self.T_max = codec, F, K, T_max
         self.epilogue, self.out = QGEMM_EPILOGUE_SWIGLU, out
         dev = torch.device(device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         nbytes = qgemm_pair_packed_bytes(F, K, codec)
         if nbytes == 0:
             raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_pair_packed_bytes")

@@ -48,24 +48,16 @@ static int route_tokens(int route) {
 }
 
 // Narrowest tile that covers T (the padded width sets the cost, not the live
-// column count).
-static int env_route() {
-    // QGEMM_ROUTE forces a route wherever its token tile covers T (for route
-    // sweeps only; unset in normal use)
-    const char *v = getenv("QGEMM_ROUTE");
-    return (v && *v) ? atoi(v) : -1;
-}
-
-static int choose_route(int T) {
-    static const int forced = env_route();
-    if (forced == ROUTE_WIDE128) return ROUTE_WIDE128;
-    if (forced == ROUTE_SKINNY32 && T <= 32) return ROUTE_SKINNY32;
-    if (forced == ROUTE_SKINNY16 && T <= 16) return ROUTE_SKINNY16;
+// column count).  A route forced on the plan (qgemm_plan_force_route) takes
+// every T its token tile covers.
+static int table_route(int T) {
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
     if (T <= 32) return ROUTE_SKINNY32;
     return ROUTE_WIDE128;
 }
+
+static bool route_covers(int route, int T) { return route == ROUTE_WIDE128 || T <= route_tokens(route); }
 
 struct qgemm_plan_s {
     int N, K, codec, T_max;
@@ -74,11 +66,16 @@ struct qgemm_plan_s {
     int G, NB, UB;
     int sms;
     bool pdl;              // launch with programmatic dependent launch
+    int forced_route;      // -1: the route table; else qgemm_plan_force_route's route
     size_t ws_bytes;       // workspace the plan's routes need (none so far)
     const uint8_t *packed;
     uint8_t *ws;
     bool bound;
 };
+
+static int choose_route(const qgemm_plan_s *p, int T) {
+    return (p->forced_route >= 0 && route_covers(p->forced_route, T)) ? p->forced_route : table_route(T);
+}
 
 static std::atomic<uint64_t> g_launches{0};
 
@@ -175,6 +172,7 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     p->UB = unit_bytes(codec);
     p->sms = sms;
     p->pdl = true;
+    p->forced_route = -1;
     p->ws_bytes = 0;
     *out = p;
     return QGEMM_OK;
@@ -242,7 +240,13 @@ qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable) {
 
 int qgemm_plan_route(qgemm_plan_t plan, int T) {
     if (!plan || T < 1 || T > plan->T_max) return -1;
-    return choose_route(T);
+    return choose_route(plan, T);
+}
+
+qgemm_status qgemm_plan_force_route(qgemm_plan_t plan, int route) {
+    if (!plan || route < -1 || route >= ROUTE_COUNT) return QGEMM_ERR_INVALID_ARG;
+    plan->forced_route = route;
+    return QGEMM_OK;
 }
 
 const char *qgemm_route_name(int route) {
@@ -291,21 +295,11 @@ static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, void *Y, const 
     sp.ybf16 = p->out == QGEMM_OUT_BF16;
 }
 
-// Tuning knob read once from the environment, for sweeps only:
-// QGEMM_SKINNY_WARPS sets the warps (K slices) per CTA of the small-T ring
-// kernel; QGEMM_SKINNY_LINE selects the groups per warp of the straight-line
-// kernel (16 or 8; 0 keeps the ring kernel).
-static int env_int(const char *name, int dflt) {
-    const char *v = getenv(name);
-    return (v && *v) ? atoi(v) : dflt;
-}
-
 // One or more parents over the same X in one launch of the route T selects.
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
                                 void *const *Ys, const float *R, cudaStream_t stream) {
-    static const int kw = env_int("QGEMM_SKINNY_WARPS", 8);
-    static const int line = env_int("QGEMM_SKINNY_LINE", 8);
-    const int route = choose_route(T);
+    // parents of one launch share its route: the first plan's choice
+    const int route = choose_route(plans[0], T);
     const int K = plans[0]->K;
     const int G = K / GROUP;
     unsigned int *status = status_ptr();
@@ -345,9 +339,11 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     a.G = G;
     bool f8 = false;
     for (int i = 0; i < np; ++i) f8 = f8 || plans[i]->codec == QGEMM_FP8;
-    const int nj = skinny_line_groups(G, line);
+    // the straight-line kernel (8 groups per warp, all in flight) where K / 64
+    // is a multiple of 8, else the ring kernel with 8 warps per CTA
+    const int nj = skinny_line_groups(G, 8);
     const cudaError_t e = nj ? launch_skinny_line(a, route_tokens(route) / 8, nj, grid, pdl, f8, stream)
-                             : launch_skinny(a, route_tokens(route) / 8, kw, grid, pdl, f8, stream);
+                             : launch_skinny(a, route_tokens(route) / 8, 8, grid, pdl, f8, stream);
     if (e != cudaSuccess) return QGEMM_ERR_CUDA;
     g_launches.fetch_add(1);
     return QGEMM_OK;

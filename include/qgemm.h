@@ -79,13 +79,17 @@ typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5, QGEMM_FP8 = 8 } qgemm_codec;
 
 typedef struct qgemm_plan_s *qgemm_plan_t;
 
-/* Human-readable name of a status (static string, never NULL). */
+/* Human-readable name of a status (static string, never NULL).
+ * Passage: none; a library convention. */
 const char *qgemm_status_string(qgemm_status st);
 
 /*
  * Bytes of the device-side packed weight buffer for an N x K matrix of the
  * given codec, or 0 for an invalid shape (K not a positive multiple of 64,
  * N < 1, unknown codec).  Rows are padded to a multiple of 128.
+ * Passage: the count of scales follows the one scale per 64 K-columns per row
+ * of "ninfer-3080 docs/performance.md" (cuBLAS prefill route section); the
+ * device layout itself is the library's own (see qgemm_pack_weights).
  */
 size_t qgemm_packed_bytes(int N, int K, qgemm_codec codec);
 
@@ -98,6 +102,13 @@ size_t qgemm_packed_bytes(int N, int K, qgemm_codec codec);
  *   scales_fp16_dev      fp16 patterns [N][K/64]
  *   packed_dev           qgemm_packed_bytes(N, K, codec) bytes, 16-byte aligned
  * The inputs may be freed once the stream has passed the launch.
+ * Passage: "ninfer-3080 docs/performance.md", small-T kernels section: the
+ * k slots of an MMA may be any permutation of a group as long as both
+ * operands agree, and the Q5 codec keeps a separate high-bit plane; the token
+ * tile section notes that the operand layout lever needs a repack, which this
+ * call performs once at load time.
+ * Errors: QGEMM_ERR_INVALID_ARG (unknown codec, NULL pointer), QGEMM_ERR_SHAPE,
+ * QGEMM_ERR_ALIGNMENT (packed_dev), QGEMM_ERR_CUDA (launch failure).
  */
 qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
                                 const void *codes_canonical_dev,
@@ -110,11 +121,21 @@ qgemm_status qgemm_pack_weights(qgemm_codec codec, int N, int K,
  * "ninfer-3080 docs/performance.md" route boundaries section explains why
  * boundaries must come from measurement).  Queries the current device's SM
  * count; launches nothing.  *out must be released with qgemm_plan_destroy.
+ * Passage: "ninfer-3080 docs/performance.md", route boundaries section: each
+ * schedule has an explicit domain of column counts, boundaries are measured
+ * rather than inherited, and the narrowest tile covering the extent wins;
+ * T_max is this plan's domain (qgemm_run rejects T > T_max).
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL out, unknown codec, T_max < 1),
+ * QGEMM_ERR_SHAPE (N < 1 or K not a positive multiple of 64),
+ * QGEMM_ERR_UNSUPPORTED (no CUDA device).
  */
 qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t *out);
 
 /* Workspace bytes the plan needs at its T_max (0 if none; the current
- * routes combine their K splits on chip and need none). */
+ * routes combine their K splits on chip and need none).  NULL plan: 0.
+ * Passage: "ninfer-3080 docs/performance.md", small-T kernels section
+ * (split-K across CTAs measured not worth a workspace); the query itself is a
+ * library convention. */
 size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan);
 
 /*
@@ -122,6 +143,12 @@ size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan);
  * be zero-filled before its first use (the library leaves it zeroed after
  * every completed run).  Runs that share one plan, and hence one workspace,
  * must not overlap on the GPU.  ws_bytes may exceed the requirement.
+ * The plan keeps both pointers; the caller keeps them alive and unchanged for
+ * as long as runs of the plan may execute.
+ * Passage: none; a library convention (weights are packed once and bound to
+ * the plan, so a run takes only X, T and Y).
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL plan or packed_dev),
+ * QGEMM_ERR_ALIGNMENT, QGEMM_ERR_WORKSPACE.
  */
 qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev,
                              void *workspace_dev, size_t ws_bytes);
@@ -131,6 +158,14 @@ qgemm_status qgemm_plan_bind(qgemm_plan_t plan, const void *packed_dev,
  * must be 16-byte aligned.  T == 0 is a no-op; T > T_max returns
  * QGEMM_ERR_T_OUT_OF_DOMAIN.  The plan must have the default output (STORE,
  * F32; see qgemm_plan_set_epilogue), else QGEMM_ERR_INVALID_ARG.
+ * X holds at least T*K bf16 values and Y at least T*N floats: the library
+ * sees only pointers and cannot check their extents.
+ * Passage: the one-pass unpack-and-multiply of "Fused kernels" (section "Why
+ * standard kernels stall"), over the token widths of "ninfer-3080
+ * docs/performance.md" (route boundaries section: a decode round covers
+ * concurrency x (draft window + 1) columns; prefill chunks are wider).
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL or unbound plan, NULL X/Y with T > 0,
+ * T < 0), QGEMM_ERR_T_OUT_OF_DOMAIN, QGEMM_ERR_ALIGNMENT, QGEMM_ERR_CUDA.
  */
 qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_stream_t stream);
 
@@ -147,7 +182,9 @@ qgemm_status qgemm_run(qgemm_plan_t plan, const void *X, int T, float *Y, qgemm_
 qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents, const void *X, int T,
                              float *const *Ys, qgemm_stream_t stream);
 
-/* Release a plan (NULL is accepted). */
+/* Release a plan (NULL is accepted).  Runs already enqueued keep working:
+ * they hold copies of what they need.
+ * Passage: none; a library convention. */
 qgemm_status qgemm_plan_destroy(qgemm_plan_t plan);
 
 /*
@@ -219,20 +256,39 @@ qgemm_status qgemm_run_ex(qgemm_plan_t plan, const void *X, int T, const void *R
  * be written by the kernel immediately preceding a run on the same stream
  * (qgemm_pack_weights itself ends with an empty kernel for this reason).
  * enable = 0 turns it off for runs of this plan.
+ * Passage: "ninfer-3080 docs/performance.md", small-T kernels section: what
+ * is left at one stream is ramp-up and drain at kernel boundaries, and
+ * programmatic dependent launch is the lever named for hiding the ramp.
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL plan).
  */
 qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable);
 
 /*
  * Route the plan takes at width T (a small integer naming the kernel family
  * and its tile width, see qgemm_route_name), or -1 if T is outside 1..T_max.
+ * Passage: "ninfer-3080 docs/performance.md", route boundaries section (the
+ * cost of a route is set by its padded tile width).
  */
 int qgemm_plan_route(qgemm_plan_t plan, int T);
 const char *qgemm_route_name(int route);
 
 /*
+ * Route sweeps and tests: make the plan take `route` at every T its token
+ * tile covers (the other T keep the built-in table); -1 restores the table.
+ * Results stay within the accuracy contract on every route, and a forced
+ * plan is bitwise repeatable for a given T like any other.
+ * Passage: "ninfer-3080 docs/performance.md", route boundaries section (every
+ * schedule of an Op is timed at the same column count to place a boundary).
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL plan, route outside -1 .. routes - 1).
+ */
+qgemm_status qgemm_plan_force_route(qgemm_plan_t plan, int route);
+
+/*
  * Number of kernels this library has launched since it was loaded (host
  * counter), so that callers and tests can check that one call runs exactly
  * the kernels its route names.
+ * Passage: "ninfer-3080 docs/performance.md", route boundaries section (a
+ * dispatch fallthrough once ran a second kernel after the first).
  */
 uint64_t qgemm_launch_count(void);
 
@@ -240,6 +296,7 @@ uint64_t qgemm_launch_count(void);
  * Device-side status word: QGEMM_OK, or QGEMM_ERR_TIMEOUT after a bounded
  * wait inside a kernel ran out (the kernel then skipped its remaining work
  * and returned).  Synchronises `stream` to read it; `clear` resets it.
+ * Passage: none; a library convention (bounded waits instead of hangs).
  */
 qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear);
 
@@ -250,6 +307,7 @@ qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear);
  * as any kernel does when one of its waits runs out.  The kernel faults
  * nothing and leaves the context usable; read and clear the word with
  * qgemm_device_status.  Returns QGEMM_ERR_CUDA if the launch fails.
+ * Passage: none; a library diagnostic.
  */
 qgemm_status qgemm_selftest_timeout(qgemm_stream_t stream);
 

@@ -21,5 +21,5 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["steps"] == 500 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
-    assert line["config"]["workload"] == "decode"
+    assert line["config"]["workload"] == "all"
     assert time.time() - t0 < 120          # the budget, not the step count, sets the time

@@ -16,6 +16,7 @@ import pytest
 
 import oracle
 from bit_weight_only_groupwise_gb300 import synth
+from tests.oracle_columns import gemm_columns, wide_columns
 from tests.tolerance import assert_close
 
 torch = pytest.importorskip("torch")
@@ -37,17 +38,9 @@ def make_weights(parent, T_max):
     return qg.GroupwiseWeights(parent["bits"], parent["N"], parent["K"], parent["packed"], parent["scales"], T_max)
 
 
-def column_subset(T, m, seed=0):
-    if T <= m:
-        return np.arange(T)
-    rng = np.random.default_rng(seed + T)
-    pick = rng.choice(np.arange(1, T - 1), size=m - 2, replace=False)
-    return np.unique(np.concatenate([[0, T - 1], pick]))
-
-
 def check_against_oracle(parent, x, Y, cols=None, what=""):
     xs = x if cols is None else x[cols]
-    Yref, A = oracle.gemm_parent(parent, xs)
+    Yref, A = gemm_columns(parent, xs)
     Yg = y_host(Y)
     if cols is not None:
         Yg = Yg[cols]
@@ -95,7 +88,7 @@ def test_batched_widths(batched_weights, T):
     p, W = batched_weights
     x = synth.activations(0, T, 5120, outliers=True)
     Y = W.run(dev_x(x))
-    check_against_oracle(p, x, Y, cols=column_subset(T, 12), what=f"batched T={T}")
+    check_against_oracle(p, x, Y, cols=wide_columns(T), what=f"batched T={T}")
 
 
 @pytest.mark.parametrize("T", [4, 16, 64])
@@ -105,7 +98,7 @@ def test_multi_parent_shared_activation(T):
     Ws = [make_weights(p, T_max=64) for p in ps]
     X = dev_x(wl["x"])
     Ys = qg.run_multi(Ws, X)
-    cols = column_subset(T, 8)
+    cols = wide_columns(T)
     for p, Y in zip(ps, Ys):
         check_against_oracle(p, wl["x"], Y, cols=cols, what=f"multi T={T} int{p['bits']}")
     # each parent alone: a different launch (its own split count), so the same
@@ -124,7 +117,7 @@ def test_prefill_widths(name, N, K, T):
     W = make_weights(p, T_max=T)
     x = synth.activations(0, T, K, outliers=True)
     Y = W.run(dev_x(x))
-    check_against_oracle(p, x, Y, cols=column_subset(T, 6), what=f"{name} T={T}")
+    check_against_oracle(p, x, Y, cols=wide_columns(T), what=f"{name} T={T}")
 
 
 # ------------------------------------------------------------ edge cases
@@ -232,8 +225,8 @@ def test_negated_scales_and_repeatability(T):
 
 @pytest.mark.parametrize("bits,T", [(5, 32), (4, 64), (5, 8)])
 def test_repeatable_when_the_stage_ring_wraps(bits, T):
-    # 12288 rows leave few K splits per block, so each CTA streams many more
-    # units than its ring holds: the slot reuse and cluster combine must stay exact
+    # 12288 rows x 5120 columns: each warp or CTA streams many more units than
+    # its ring holds, so slot reuse must stay exact across the wraps
     p = synth.weights(10, 12288, 5120, bits)
     W = make_weights(p, T_max=64)
     x = synth.activations(10, T, 5120, outliers=True)

@@ -62,3 +62,18 @@ def test_pack_canonical_layout():
     c5 = np.zeros((1, 8), np.int8)
     c5[0, 1] = -1
     assert synth.pack_canonical(c5, 5).tolist() == [[0xE0, 0x03, 0, 0, 0]]
+
+
+def test_column_parallel_oracle_equals_one_call():
+    # the parity tests' thread-pool split of the oracle over token columns
+    # gives exactly the single-call result (the oracle is column-independent)
+    import oracle
+    from tests.oracle_columns import gemm_columns, wide_columns
+    p = synth.weights(4, 37, 192, 5)
+    x = synth.activations(4, 29, 192, outliers=True)
+    Y1, A1 = oracle.gemm_parent(p, x)
+    Y2, A2 = gemm_columns(p, x, chunk=4)
+    assert np.array_equal(Y1, Y2) and np.array_equal(A1, A2)
+    assert np.array_equal(wide_columns(200), np.arange(200))
+    c = wide_columns(4096)
+    assert c[0] == 0 and c[-1] == 4095 and np.all(np.isin(np.arange(0, 4096, 64), c)) and len(c) >= 64

@@ -20,8 +20,10 @@ cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pd
 int skinny_line_groups(int G, int nj_pref);
 cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, bool f8,
                                cudaStream_t stream);
-cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
-                        cudaStream_t stream, int *launches);
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int halves, float *part,
+                        unsigned int *status, bool pdl, int sms, cudaStream_t stream);
+size_t wide_workspace_bytes(int rows, int T_max, int sms);
+size_t wide_partial_bytes(int T_max, int sms);
 }  // namespace qg
 
 using namespace qg;
@@ -32,20 +34,25 @@ enum Route : int {
     ROUTE_SKINNY8 = 0,     // weight-streaming skinny GEMM, 8-token MMA tile
     ROUTE_SKINNY16 = 1,    // 16-token tile
     ROUTE_SKINNY32 = 2,    // 32-token tile
-    ROUTE_WIDE128 = 3,     // tcgen05 tiles of 128 rows x 128 tokens
+    ROUTE_WIDE128 = 3,     // stream-K tcgen05 tiles of 128 rows x 128 tokens
+    ROUTE_WIDE256 = 4,     // stream-K tcgen05 tiles of 128 rows x 256 tokens (two 128-token halves)
     ROUTE_COUNT
 };
 
-static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "tcgen05_128x128"};
+static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "tcgen05_128x128",
+                                               "tcgen05_128x256"};
 
 static int route_tokens(int route) {
     switch (route) {
         case ROUTE_SKINNY8: return 8;
         case ROUTE_SKINNY16: return 16;
         case ROUTE_SKINNY32: return 32;
-        default: return 128;
+        case ROUTE_WIDE128: return 128;
+        default: return 256;
     }
 }
+
+static bool wide_route(int route) { return route == ROUTE_WIDE128 || route == ROUTE_WIDE256; }
 
 // Narrowest tile that covers T (the padded width sets the cost, not the live
 // column count).  A route forced on the plan (qgemm_plan_force_route) takes
@@ -54,10 +61,12 @@ static int table_route(int T) {
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
     if (T <= 32) return ROUTE_SKINNY32;
-    return ROUTE_WIDE128;
+    if (T <= 128) return ROUTE_WIDE128;
+    return ROUTE_WIDE256;
 }
 
-static bool route_covers(int route, int T) { return route == ROUTE_WIDE128 || T <= route_tokens(route); }
+// the tcgen05 routes walk any number of token tiles
+static bool route_covers(int route, int T) { return wide_route(route) || T <= route_tokens(route); }
 
 struct qgemm_plan_s {
     int N, K, codec, T_max;
@@ -67,7 +76,8 @@ struct qgemm_plan_s {
     int sms;
     bool pdl;              // launch with programmatic dependent launch
     int forced_route;      // -1: the route table; else qgemm_plan_force_route's route
-    size_t ws_bytes;       // workspace the plan's routes need (none so far)
+    size_t ws_bytes;       // workspace the plan's routes need (the tcgen05 routes' split tiles)
+    size_t ws_part;        // of it, the partial-sum slots (the counters follow)
     const uint8_t *packed;
     uint8_t *ws;
     bool bound;
@@ -173,7 +183,8 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     p->sms = sms;
     p->pdl = true;
     p->forced_route = -1;
-    p->ws_bytes = 0;
+    p->ws_bytes = wide_workspace_bytes(N, T_max, sms);
+    p->ws_part = p->ws_bytes ? wide_partial_bytes(T_max, sms) : 0;
     *out = p;
     return QGEMM_OK;
 }
@@ -229,6 +240,8 @@ qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue,
     plan->out = out;
     plan->rows = epilogue == QGEMM_EPILOGUE_SWIGLU ? pair_rows(plan->N) : plan->N;
     plan->NB = (plan->rows + BLOCK_ROWS - 1) / BLOCK_ROWS;
+    plan->ws_bytes = wide_workspace_bytes(plan->rows, plan->T_max, plan->sms);
+    plan->ws_part = plan->ws_bytes ? wide_partial_bytes(plan->T_max, plan->sms) : 0;
     return QGEMM_OK;
 }
 
@@ -243,8 +256,17 @@ int qgemm_plan_route(qgemm_plan_t plan, int T) {
     return choose_route(plan, T);
 }
 
+// Whether the plan's workspace holds what `route` needs: the tcgen05 routes
+// keep partial sums sized by T_max (128-token tiles above T_max = 32,
+// 256-token tiles above 128).
+static bool workspace_fits(const qgemm_plan_s *p, int route) {
+    if (!wide_route(route)) return true;
+    return p->T_max > 32 && (route == ROUTE_WIDE128 || p->T_max > 128);
+}
+
 qgemm_status qgemm_plan_force_route(qgemm_plan_t plan, int route) {
     if (!plan || route < -1 || route >= ROUTE_COUNT) return QGEMM_ERR_INVALID_ARG;
+    if (route >= 0 && !workspace_fits(plan, route)) return QGEMM_ERR_INVALID_ARG;
     plan->forced_route = route;
     return QGEMM_OK;
 }
@@ -304,26 +326,31 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     const int G = K / GROUP;
     unsigned int *status = status_ptr();
     if (!status) return QGEMM_ERR_CUDA;
-    if (route == ROUTE_WIDE128) {
+    bool pdl = true;
+    for (int i = 0; i < np; ++i) pdl = pdl && plans[i]->pdl;
+    if (wide_route(route)) {
+        for (int i = 0; i < np; ++i)
+            if (!workspace_fits(plans[i], route)) return QGEMM_ERR_INVALID_ARG;
         WideParent wp[MAX_PARENTS];
         memset(wp, 0, sizeof wp);
         for (int i = 0; i < np; ++i) {
             wp[i].packed = plans[i]->packed;
             wp[i].Y = Ys[i];
             wp[i].R = R;
+            wp[i].cnt = reinterpret_cast<unsigned int *>(plans[i]->ws + plans[i]->ws_part);
             wp[i].N = plans[i]->rows;
             wp[i].codec = plans[i]->codec;
             wp[i].ncols = plans[i]->N;
             wp[i].epi = plans[i]->epi;
             wp[i].ybf16 = plans[i]->out == QGEMM_OUT_BF16;
         }
-        int launches = 0;
-        if (launch_wide(wp, np, X, T, K, status, stream, &launches) != cudaSuccess) return QGEMM_ERR_CUDA;
-        g_launches.fetch_add(launches);
+        // the partial-sum slots of the first parent's workspace serve the launch
+        if (launch_wide(wp, np, X, T, K, route == ROUTE_WIDE256 ? 2 : 1, reinterpret_cast<float *>(plans[0]->ws),
+                        status, pdl, plans[0]->sms, stream) != cudaSuccess)
+            return QGEMM_ERR_CUDA;
+        g_launches.fetch_add(1);
         return QGEMM_OK;
     }
-    bool pdl = true;
-    for (int i = 0; i < np; ++i) pdl = pdl && plans[i]->pdl;
     SkinnyArgs a;
     memset(&a, 0, sizeof a);
     int grid = 0;

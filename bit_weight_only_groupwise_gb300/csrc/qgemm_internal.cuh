@@ -101,11 +101,13 @@ struct SkinnyArgs {
     unsigned int *status;    // device status word
 };
 
-// The wide route covers ceil(N/128) x ceil(T/128) output tiles per parent.
+// The wide route covers ceil(N/128) x ceil(T/BN) output tiles per parent
+// (BN = 128 or 256 tokens).
 struct WideParent {
     const uint8_t *packed;   // units of this parent
     void *Y;                 // [T][ncols], fp32 or bf16
     const float *R;          // EPI_ADD: residual [T][ncols]
+    unsigned int *cnt;       // this parent's split-tile counters (zero between runs)
     int N, codec;            // N: packed rows
     int cta_begin;           // first output tile of this parent in its launch
     int nblocks;             // 128-row blocks

@@ -1,41 +1,52 @@
-// Wide-T route: a tcgen05 (5th-generation tensor core) dequant-GEMM.
+// Wide-T route: a persistent, stream-K tcgen05 (5th-generation tensor core)
+// dequant-GEMM.
 //
 // From a few dozen token columns up the operation is a dense contraction and
 // belongs on the tensor cores; prefill widths are compute-bound ("ninfer-3080
 // docs/performance.md", token tile section: the token tile width sets how
 // often the weights are re-streamed, and the per-group rescale and the operand
-// assembly are the costs beside the MMAs).  One CTA computes a 128-row block of
-// Y^T for a 128-token tile:
+// assembly are the costs beside the MMAs).  An output tile is 128 weight rows
+// by BN = 128 or 256 tokens:
 //
-//   D[128 rows x 128 tokens] = sum over 64-column groups g of s[:, g] * P_g,
-//   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, 128 x 64)^T
+//   D[128 rows x BN tokens] = sum over 64-column groups g of s[:, g] * P_g,
+//   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, BN x 64)^T
+//
+// A 256-token tile runs as two 128-token halves over the same decoded A_g, so
+// each decoded weight feeds twice the tensor work (the page's lesson: wider
+// token tiles remove weight passes, they are not cached away).
+//
+// Work split (stream-K): the (tile, group) units of all parents of the launch
+// are numbered tile-major and cut into one contiguous range per CTA, one CTA
+// per SM, so every SM gets the same number of groups whatever the tile count.
+// A tile whose groups span several CTAs is finished by the CTA that completes
+// it last: the others leave their fp32 partial sums in the workspace and
+// count in, and the last one adds them in ascending CTA order (a fixed order,
+// so results are bitwise repeatable) and writes Y.  No CTA waits for another.
 //
 // Warp roles (16 warps; every single-issuer role is a converged warp whose
 // elected lane issues, and every wait is taken by the whole warp):
-//   warp 0        weight producer: 1-D bulk copies of the packed units into a
-//                 deep smem ring;
-//   warp 1        allocates tensor memory and issues the MMAs of even
-//                 groups; warp 3 issues those of odd groups;
+//   warp 0        weight producer: 1-D bulk copies of pairs of packed units
+//                 into a shared-memory ring (the only role that runs before
+//                 the programmatic wait on the previous kernel);
+//   warps 1, 3    MMA issuers (alternate steps; warp 1 also owns tensor
+//                 memory);
 //   warp 2        activation producer: 2-D TMA loads of 128B-swizzled X tiles;
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
-//                 the group (magic-number bf16 decode, exact) and stores them
-//                 into tensor memory as the A operand (tcgen05.st), so shared
-//                 memory bandwidth is left to the B operand; the row's scale
-//                 goes to the epilogue through a small shared-memory ring;
-//   warps 8..15   epilogue: read P_g from tensor memory (tcgen05.ld), multiply
+//                 a group (magic-number bf16 decode, exact) into tensor memory
+//                 as the A operand (tcgen05.st); the row's scale goes to the
+//                 epilogue through a shared-memory ring;
+//   warps 8..15   epilogue: read P from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
-//                 (packed f32x2 FMA), then write Y.
-// Tensor memory: NP P buffers of 128 columns (the MMA fills one while the
-// epilogue drains another) and NA A stages of 32 columns (64 bf16 per row).
-// Synchronisation per group g (stage s = g mod NS):
-//   go[s]     completes when A_g is in tensor memory (4 dequant arrivals),
-//             X_g has landed (TMA transaction bytes + 1 arrival) and the P
-//             buffer of g is drained (8 epilogue arrivals after group g - NP):
-//             the MMA warp waits on this one barrier per group;
-//   done[s]   the MMA commit of group g: P_g is complete (the epilogue waits
-//             on it) and A and X stage s may be overwritten (the dequant and
-//             the activation producer wait on it for group g + NS); one
-//             commit per group, as every MMA issue costs the issuing thread.
+//                 (packed f32x2 FMA); write Y, or a partial sum and its count.
+// A step is one 128-token half of one group: step j = unit * H + h.
+// Tensor memory: NP = 3 P buffers of 128 columns (step j uses j mod 3, so
+// the epilogue has two steps of MMA time to drain a buffer) and NA = 4 A
+// stages of 32 columns.  Barriers:
+//   xa_full[s]   A_g stored (4 dequant warps) and X_g landed (TMA bytes)
+//   xa_empty[s]  the MMAs of both halves of group g completed (one commit
+//                per step): X stage s and A stage g mod NA are free
+//   pfull[b]     the MMAs of the step in P buffer b completed
+//   pfree[b]     the 8 epilogue warps have read P buffer b
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // to timeout and the CTA winds down (after a bounded pause that lets copies
 // and MMAs already issued land before tensor memory is released).
@@ -49,38 +60,44 @@ namespace qg {
 
 namespace wide {
 
-constexpr int BM = 128;                   // weight rows per CTA (TMEM lanes)
-constexpr int BN = 128;                   // tokens per CTA (MMA N)
-constexpr int NS = 8;                     // activation stages (and the go / done ring)
-constexpr int NA = 8;                     // A stages in tensor memory (group g uses g % NA)
-constexpr int NWP = 8;                    // weight stages, each a pair of consecutive groups' units
-constexpr int NP = 2;                     // P buffers in tensor memory
-constexpr int DQ_WARPS = 4;               // one dequant warp per TMEM lane quarter
+constexpr int BM = 128;                   // weight rows per tile (tensor-memory lanes)
+constexpr int BH = 128;                   // tokens per MMA: one half of a 256-token tile
+constexpr int NA = 4;                     // A stages in tensor memory (unit u uses u mod NA)
+constexpr int NP = 3;                     // P buffers in tensor memory (step j uses j mod NP)
+constexpr int DQ_WARPS = 4;               // one dequant warp per tensor-memory lane quarter
 constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
 constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
 constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
-constexpr int GO_COUNT = DQ_WARPS + 1 + EPI_WARPS;
-constexpr int SC_RING = 16;               // groups of scales in flight
-// the dequant stores the scale of group g once the epilogue has finished group g - NS - NP - 1
-static_assert(SC_RING >= NA + NP + 2, "scale ring shorter than the dequant lead");
-static_assert(NA <= NS && NA % 2 == 0, "A stages: even (pairs of groups) and no more than the ring");
-static_assert(NS > NP, "go barrier phases need more stages than P buffers");
-constexpr int X_STAGE = BN * GROUP * 2;   // 16 KB
-constexpr int P_COL = 0;                  // P buffers: columns [0, 128*NP)
-constexpr int A_COL = NP * BN;            // A stages: columns [128*NP, 128*NP + 32*NA)
-static_assert(A_COL + 32 * NA <= 512, "tensor memory budget");
+constexpr int SC_RING = 16;               // units of scales in flight
+constexpr int P_COL = 0;                  // P buffers: columns [0, 128 NP)
+constexpr int A_COL = NP * BH;            // A stages: columns [128 NP, 128 NP + 32 NA)
 constexpr int TMEM_COLS = 512;
+static_assert(A_COL + 32 * NA <= TMEM_COLS, "tensor memory budget");
+constexpr int X_REGION = 128 * 1024;      // activation stages
+constexpr int HALF_BYTES = BH * GROUP * 2;   // 16 KB: one half's X tile of one group
+// the dequant stores the scale of unit u + 1 once the MMAs of unit u - 1 - NA
+// are done, and those waited for the epilogue of three steps earlier
+static_assert(SC_RING >= NA + NP + 3, "scale ring shorter than the dequant lead");
 
-struct Smem {
-    static constexpr int X_OFF = 0;                          // 1024-aligned (128B swizzle atoms)
-    static constexpr int W_OFF = X_OFF + NS * X_STAGE;
-    static constexpr int BAR_OFF = W_OFF + NWP * 2 * UNIT5;
-    static constexpr int NBAR = 2 * NWP + 2 * NS;
-    static constexpr int SC_OFF = BAR_OFF + NBAR * 8;                 // float [SC_RING][BM]
-    static constexpr int TADDR_OFF = SC_OFF + SC_RING * BM * 4;
-    static constexpr int BYTES = TADDR_OFF + 16 + 1024;      // + slack to align the base
+// H: halves per tile (BN = 128 H tokens); F8: a parent of the launch holds
+// FP8 codes (larger units, so fewer weight stages fit).
+template <int H, bool F8>
+struct Geo {
+    static constexpr int BN = H * BH;
+    static constexpr int XST = H * HALF_BYTES;           // X stage: BN tokens x 64 columns
+    static constexpr int NS = X_REGION / XST;             // 8 stages (H = 1) or 4 (H = 2)
+    static constexpr int WSLOT = 2 * (F8 ? UNIT8 : UNIT5);
+    static constexpr int NWP = F8 ? 4 : 6;                // weight stages (pairs of units)
+    static constexpr int X_OFF = 0;                       // 1024-aligned (128B swizzle atoms)
+    static constexpr int W_OFF = X_REGION;
+    static constexpr int BAR_OFF = W_OFF + NWP * WSLOT;
+    static constexpr int NBAR = 2 * NWP + 2 * NS + 2 * NP;
+    static constexpr int SC_OFF = BAR_OFF + NBAR * 8;     // float [SC_RING][BM]
+    static constexpr int MISC_OFF = SC_OFF + SC_RING * BM * 4;
+    static constexpr int BYTES = MISC_OFF + 16 + 1024;    // + slack to align the base
+    static_assert(NS >= NA, "A stages are recycled through the X stage barriers");
+    static_assert(BYTES <= 227 * 1024, "shared memory budget");
 };
-static_assert(Smem::BYTES <= 227 * 1024, "shared memory budget");
 
 }  // namespace wide
 
@@ -88,15 +105,17 @@ struct WideArgs {
     WideParent p[MAX_PARENTS];
     int nparents;
     int T, K, G;
-    int ntt;              // token tiles
+    int ntt;              // token tiles of BN tokens
     int ntiles;           // output tiles of all parents (parent i owns p[i].cta_begin ...)
+    long long units;      // ntiles * G
+    float *part;          // partial sums of split tiles: [grid][2][BN][BM]
     unsigned int *status;
 };
 
-// An output tile: its parent, 128-row block and 128-token tile.
+// An output tile: its parent, 128-row block and token tile.
 struct WideTile {
     const WideParent *P;
-    int blk, tt;
+    int local, blk, tt;
 };
 
 __device__ __forceinline__ WideTile wide_tile(const WideArgs &a, int tile) {
@@ -105,7 +124,15 @@ __device__ __forceinline__ WideTile wide_tile(const WideArgs &a, int tile) {
     for (int i = 1; i < MAX_PARENTS; ++i)
         if (i < a.nparents && tile >= a.p[i].cta_begin) pi = i;
     const int local = tile - a.p[pi].cta_begin;
-    return {&a.p[pi], local / a.ntt, local % a.ntt};
+    return {&a.p[pi], local, local / a.ntt, local % a.ntt};
+}
+
+// Stream-K ranges: CTA c owns units [lo(c), lo(c + 1)), lo(c) = floor(c U / grid);
+// every CTA owns at least one unit when grid <= U.
+__device__ __forceinline__ long long range_lo(long long U, int grid, int c) { return (long long)c * U / grid; }
+// the CTA whose range holds unit u
+__device__ __forceinline__ int range_cta(long long U, int grid, long long u) {
+    return (int)(((u + 1) * grid - 1) / U);
 }
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -201,11 +228,146 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return *reinterpret_cast<float2 *>(&d);
 }
 
-// ---------------------------------------------------------------- the kernel
+// Register budgets per warpgroup: the epilogue keeps up to 128 fp32
+// accumulators per thread and reads a split tile's partials beside them, so
+// the producer, MMA and dequant warps give registers up for it.  The block
+// launches with 512 threads x 128 registers (65,536); the shares below add up
+// to 128 x (40 + 128) + 256 x 168 or 128 x (40 + 96) + 256 x 184 = 64,512.
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+// The 128-token tile's dequant decodes a pair of units at once (more
+// registers); the 256-token tile's epilogue holds twice the accumulators.
+constexpr int REGS_LAUNCH = 128, REGS_WG0 = 40;
+template <int H> struct Regs {
+    static constexpr int DQ = H == 1 ? 128 : 96;
+    static constexpr int EPI = H == 1 ? 168 : 184;
+    static_assert(128 * (REGS_WG0 + DQ) + 256 * EPI <= 512 * REGS_LAUNCH, "register split");
+};
 
-// Fused outputs of one tile's accumulators (thread = row n, tokens t0 + 2j,
-// t0 + 2j + 1): residual add, bf16, or SwiGLU, where lanes l and l + 8 hold
-// the gate and the up row of one output.
+// ---------------------------------------------------------------- dequant
+
+// Weight row r of a unit in shared memory as 32 bf16x2 words in natural k
+// order (word m = columns 2m, 2m + 1), and its fp16 scale.
+template <int CODEC>
+__device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&av)[32]) {
+    const int tile = r >> 4, i = r & 15, gi_ = i & 7, half = i >> 3;
+    if constexpr (CODEC == 8) {
+        // E4M3: the row's 16 codes of lane chunk c (k 16c .. 16c+15)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(u + tile * 1024 + (4 * gi_ + c) * 32 + 16 * half);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) {
+                av[8 * c + 2 * j2] = dec8_pair<0>(wv[j2]);
+                av[8 * c + 2 * j2 + 1] = dec8_pair<1>(wv[j2]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi_ + c) * 16 + 8 * half);
+            const uint32_t hw = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi_ + c) * 4)
+                                           : 0u;
+            const uint32_t wv[2] = {v.x, v.y};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w = wv[h];
+                uint32_t *o = av + 8 * c + 4 * h;
+                if constexpr (CODEC == 4) {
+                    o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
+                } else {
+                    // this row's words in the lane's high word: m = 2*half + h
+                    const uint32_t hh = hw >> (4 * (2 * half + h));
+                    o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
+                    o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
+                }
+            }
+        }
+    }
+    return __half2float(*reinterpret_cast<const __half *>(u + scale_off(CODEC) + tile * 32 + gi_ * 4 + half * 2));
+}
+
+// The dequant warps over one segment (units k0 .. k1 - 1 of a tile of codec
+// CODEC): pairs of units per weight stage; a unit's codes go into A stage
+// gi mod NA once the MMAs of unit gi - NA have freed it.  PAIR: both units of
+// a stage are decoded before either is stored, so that one store wait serves
+// two units (the integer codecs on the 128-token tile, where a unit's MMAs
+// are short); otherwise one unit at a time (fewer live registers: the FP8
+// decode, the 256-token tile's accumulators).
+template <int CODEC, int NS, int NWP, int WSLOT, bool PAIR>
+__device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
+                                                uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
+                                                float *sc_ring, uint32_t tmem, int q, int lane,
+                                                unsigned int *status) {
+    using namespace wide;
+    constexpr int UB = unit_bytes(CODEC);
+    const int r = q * 32 + lane;
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;
+    for (int k = k0; k < k1; k += 2, ++jp) {
+        const int wsl = jp % NWP;
+        const int n = k + 1 < k1 ? 2 : 1;
+        if (!mbar_wait_warp(&w_full[wsl], (jp / NWP) & 1, status)) return false;
+        if constexpr (PAIR) {
+            uint32_t av[2][32];
+            sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT, r, av[0]);
+            if (n == 2) sc_ring[((gi + 1) % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + UB, r, av[1]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[wsl]);
+            // A stages of both units were last read by the MMAs of units gi - NA
+            // and gi + 1 - NA
+            const int h0 = gi - NA, h1 = gi + 1 - NA;
+            bool ok = true;
+            if (n == 2 && h0 >= 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait2(&xa_empty[h0 % NS], (h0 / NS) & 1, &xa_empty[h1 % NS],
+                                                        (h1 / NS) & 1, status));
+            } else if (h0 >= 0) {
+                ok = mbar_wait_warp(&xa_empty[h0 % NS], (h0 / NS) & 1, status);
+            } else if (n == 2 && h1 >= 0) {
+                ok = mbar_wait_warp(&xa_empty[h1 % NS], (h1 / NS) & 1, status);
+            }
+            if (!ok) return false;
+            tc_fence_after();
+            tc_st32(tmem + tlane + A_COL + (gi % NA) * 32, av[0]);
+            if (n == 2) tc_st32(tmem + tlane + A_COL + ((gi + 1) % NA) * 32, av[1]);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&xa_full[gi % NS]);
+                if (n == 2) mbar_arrive(&xa_full[(gi + 1) % NS]);
+            }
+            gi += n;
+        } else {
+            for (int e = 0; e < n; ++e, ++gi) {
+                uint32_t av[32];
+                sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + e * UB, r, av);
+                if (e == n - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[wsl]);
+                }
+                // A stage gi mod NA was last read by the MMAs of unit gi - NA
+                const int h = gi - NA;
+                if (h >= 0 && !mbar_wait_warp(&xa_empty[h % NS], (h / NS) & 1, status)) return false;
+                tc_fence_after();
+                tc_st32(tmem + tlane + A_COL + (gi % NA) * 32, av);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xa_full[gi % NS]);
+            }
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- outputs
+
+// A tile's fused outputs for one thread's 64 tokens t0 .. t0 + 63 of row n
+// (acc[j] = tokens t0 + 2j, t0 + 2j + 1): residual add, bf16, or SwiGLU,
+// where lanes l and l + 8 hold the gate and the up row of one output.
 __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t0, int T, const float2 (&acc)[32]) {
     if (P.epi == EPI_SWIGLU) {
         const int f = (n >> 4) * 8 + (n & 7);
@@ -249,48 +411,104 @@ __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t
     }
 }
 
-// CODEC: the codec of every parent of the launch (4 or 5); a launch whose
-// parents mix codecs is split into one launch per codec by the host.  FUSED:
-// the launch's parent has a fused output (residual add, SwiGLU or bf16); the
-// plain instantiation keeps the store loop, and the code, of the plain GEMM
-// (the fused store code in every launch measured 12% slower at T = 4096).
-template <int CODEC, bool FUSED>
+// Write one thread's finished accumulators: row n, tokens t0 + 128 h + 64 c
+// + 2j (+1) for each half h.
+template <int H, bool FUSED>
+__device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, int T, const float2 (&acc)[H][32]) {
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int th = t0 + h * wide::BH;
+        if constexpr (FUSED) {
+            wide_fused_out(P, n, th, T, acc[h]);
+        } else if (n < P.N) {
+            float *Y = static_cast<float *>(P.Y);
+            const int N = P.ncols;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = th + 2 * j;
+                if (t < T) Y[(size_t)t * N + n] = acc[h][j].x;
+                if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[h][j].y;
+            }
+        }
+    }
+}
+
+// The sum of a split tile's partials, for one epilogue thread (row r, its
+// 64-token column block c of each half): every segment's partial, this CTA's
+// own included, is read back from the workspace and summed over the
+// segments' CTAs c_first .. c_last in ascending order, so the order does not
+// depend on which CTA finishes last.  acc is overwritten (its registers hold
+// the running sum, 32 column pairs of one segment in flight beside it).
+template <int H, int BN>
+__device__ __forceinline__ void fixup_sum(float2 (&acc)[H][32], const float *part, long long U, int grid,
+                                          int c_first, int c_last, long long u0, int c, int r) {
+    constexpr int BM = wide::BM, BH = wide::BH;
+    constexpr int CH = H == 1 ? 32 : 16;              // column pairs in flight (registers)
+#pragma unroll
+    for (int h = 0; h < H; ++h)
+#pragma unroll
+        for (int jb = 0; jb < 32; jb += CH) {
+            // a CTA's first segment sits in its slot 0, its last in slot 1
+            auto seg = [&](int cc) {
+                return part + (size_t)(cc * 2 + (range_lo(U, grid, cc) >= u0 ? 0 : 1)) * BN * BM +
+                       (size_t)(h * BH + 64 * c + 2 * jb) * BM + r;
+            };
+            const float *p0 = seg(c_first);
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                acc[h][jb + j] = make_float2(__ldcg(p0 + (size_t)(2 * j) * BM), __ldcg(p0 + (size_t)(2 * j + 1) * BM));
+            for (int cc = c_first + 1; cc <= c_last; ++cc) {
+                const float *pc = seg(cc);
+                float2 v[CH];
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    v[j] = make_float2(__ldcg(pc + (size_t)(2 * j) * BM), __ldcg(pc + (size_t)(2 * j + 1) * BM));
+#pragma unroll
+                for (int j = 0; j < CH; ++j)
+                    acc[h][jb + j] = make_float2(acc[h][jb + j].x + v[j].x, acc[h][jb + j].y + v[j].y);
+            }
+        }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+// H: 128-token halves per tile (1 or 2).  FUSED: a parent of the launch has a
+// fused output (residual add, SwiGLU or bf16); the plain instantiation keeps
+// the store loop, and the code, of the plain GEMM (the fused store code in
+// every launch measured 12% slower at T = 4096).  F8: a parent holds FP8
+// codes.  Parents of different codecs share one launch: the codec is
+// resolved per tile.
+template <int H, bool FUSED, bool F8>
 __global__ void __launch_bounds__(wide::THREADS, 1)
     wide_kernel(const __grid_constant__ WideArgs args, const __grid_constant__ CUtensorMap xmap) {
     using namespace wide;
+    using Gm = Geo<H, F8>;
+    constexpr int BN = Gm::BN, NS = Gm::NS, NWP = Gm::NWP, WSLOT = Gm::WSLOT, XST = Gm::XST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xs = smem + Smem::X_OFF;
-    uint8_t *ws = smem + Smem::W_OFF;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::BAR_OFF);
+    uint8_t *xs = smem + Gm::X_OFF;
+    uint8_t *ws = smem + Gm::W_OFF;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Gm::BAR_OFF);
     uint64_t *w_full = bars, *w_empty = w_full + NWP;
-    uint64_t *go = w_empty + NWP, *done = go + NS;
-    float *sc_ring = reinterpret_cast<float *>(smem + Smem::SC_OFF);
-    volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Smem::TADDR_OFF);
+    uint64_t *xa_full = w_empty + NWP, *xa_empty = xa_full + NS;
+    uint64_t *pfull = xa_empty + NS, *pfree = pfull + NP;
+    float *sc_ring = reinterpret_cast<float *>(smem + Gm::SC_OFF);
+    volatile uint32_t *taddr_slot = reinterpret_cast<volatile uint32_t *>(smem + Gm::MISC_OFF);
     volatile uint32_t *abort_flag = taddr_slot + 1;
 
-    // ---- this CTA's work: output tiles blockIdx.x, blockIdx.x + gridDim.x,
-    // ... of all parents (parent i owns tiles [p[i].cta_begin, p[i].cta_begin
-    // + nblocks * ntt)); every role walks the same steps gi = it * G + k over
-    // the groups k of its it-th tile, so the rings and barrier phases run on
-    // across tiles and the next tile's copies and MMAs overlap this tile's
-    // epilogue
+    // ---- this CTA's units: [lo, hi) of the tile-major (tile, group)
+    // numbering; every role walks the same units in the same order (unit
+    // index gi counts from 0 in this CTA), so rings and barrier phases run on
+    // across tile boundaries
     const int G = args.G, T = args.T;
-    const int my_tiles = (int)blockIdx.x < args.ntiles ? (args.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int steps = my_tiles * G;
-    constexpr int codec = CODEC;
-    constexpr int UB = unit_bytes(CODEC);
-    // weight stages: pairs of units; FP8 units are larger, so the same region
-    // holds fewer pairs
-    constexpr int WSLOT = 2 * UB;
-    constexpr int nwp = (NWP * 2 * UNIT5) / WSLOT < NWP ? (NWP * 2 * UNIT5) / WSLOT : NWP;
-    static_assert(nwp >= 2, "weight ring");
-
+    const long long U = args.units;
+    const long long lo = range_lo(U, gridDim.x, blockIdx.x), hi = range_lo(U, gridDim.x, blockIdx.x + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NWP; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], DQ_WARPS); }
-        for (int i = 0; i < NS; ++i) { mbar_init(&go[i], GO_COUNT); mbar_init(&done[i], 1); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&xa_full[i], DQ_WARPS + 1); mbar_init(&xa_empty[i], H); }
+        for (int i = 0; i < NP; ++i) { mbar_init(&pfull[i], 1); mbar_init(&pfree[i], EPI_WARPS); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -304,238 +522,228 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *taddr_slot;
 
-    if (warp == 0) {
-        // ---------------- weight producer: the units of groups (2j, 2j+1) of a
-        // tile in one 1-D bulk copy (a row block's units are consecutive)
-        bool ok = true;
-        int jp = 0;                                   // weight stages used so far
-        for (int it = 0; it < my_tiles && ok; ++it) {
-            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
-            const uint8_t *units = tr.P->packed + (size_t)tr.blk * G * UB;
-            for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
-                const int wsl = jp % nwp;
-                const uint32_t bytes = (2 * j + 1 < G ? 2 : 1) * UB;
-                if (jp >= nwp && !(ok = mbar_wait_warp(&w_empty[wsl], ((jp / nwp) - 1) & 1, args.status))) break;
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(&w_full[wsl], bytes);
-                    bulk_g2s(ws + wsl * WSLOT, units + (size_t)(2 * j) * UB, bytes, &w_full[wsl]);
-                }
-                __syncwarp();
-            }
-        }
-        if (!ok && lane == 0) *abort_flag = 1;
-    } else if (warp == 2) {
-        // ---------------- activation producer: 128B-swizzled X tiles, 2-D TMA
-        bool ok = true;
-        int gi = 0;
-        for (int it = 0; it < my_tiles && ok; ++it) {
-            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
-            for (int k = 0; k < G; ++k, ++gi) {
-                const int s = gi % NS;
-                if (gi >= NS && !(ok = mbar_wait_warp(&done[s], ((gi / NS) - 1) & 1, args.status))) break;
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(&go[s], X_STAGE);
-                    tma_load_2d(xs + s * X_STAGE, &xmap, k * GROUP, tr.tt * BN, &go[s]);
-                }
-                __syncwarp();
-            }
-        }
-        if (!ok && lane == 0) *abort_flag = 1;
-    } else if (warp == 1 || warp == 3) {
-        // ---------------- MMA issuers: warp 1 even steps, warp 3 odd steps.
-        // Issuing a tensor-core instruction occupies the issuing warp's
-        // scheduler for tens of cycles; two issuers on two schedulers halve
-        // what the epilogue and dequant warps sharing them lose, and
-        // consecutive groups' MMA chains (different P buffers) interleave.
-        bool ok = true;
-        const uint32_t idesc = idesc_bf16(BM, BN);
-        for (int gi = warp >> 1; gi < steps; gi += 2) {
-            const int s = gi % NS, pb = gi % NP;
-            if (!(ok = mbar_wait_warp(&go[s], (gi / NS) & 1, args.status))) break;
-            tc_fence_after();
-            const uint32_t d = tmem + P_COL + pb * BN;
-            const uint32_t a = tmem + A_COL + (gi % NA) * 32;
-            const uint32_t b0 = smem_u32(xs + s * X_STAGE);
-            // one elected lane per instruction: measured cheaper to issue than
-            // one elected block of four
-#pragma unroll
-            for (int kk = 0; kk < GROUP / 16; ++kk)
-                if (elect_one()) tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
-            if (elect_one()) tc_commit(&done[s]);
-            __syncwarp();
-        }
-        if (!ok && lane == 0) *abort_flag = 1;
-    } else if (warp >= DQ0 && warp < EPI0) {
-        // ---------------- dequant: thread = weight row r of the block; groups
-        // (2j, 2j+1) of a tile per iteration, so that one weight wait, one
-        // stage wait and one tensor-memory store wait serve two groups and the
-        // two decodes overlap
-        const int q = warp & 3;                   // TMEM lane quarter
-        const int r = q * 32 + lane;
-        const int tile = r >> 4, i = r & 15, gi_ = i & 7, half = i >> 3;
-        const int soff = scale_off(codec) + tile * 32 + gi_ * 4 + half * 2;
-        const uint32_t tlane = (uint32_t)(q * 32) << 16;
-        bool ok = true;
-        int jp = 0;                                   // weight stages used so far
-        for (int it = 0; it < my_tiles && ok; ++it) {
-            for (int j = 0; j < (G + 1) / 2; ++j, ++jp) {
-                const int g0 = it * G + 2 * j;        // step of the pair's first group
-                const bool two = 2 * j + 1 < G;
-                const int wsl = jp % nwp;
-                if (!(ok = mbar_wait_warp(&w_full[wsl], (jp / nwp) & 1, args.status))) break;
-                uint32_t av[2][32];
-                if constexpr (CODEC == 8) {
-                    // E4M3: the row's 16 codes of lane chunk c (k 16c .. 16c+15)
-                    // decoded straight from shared memory, in natural k order
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint8_t *u = ws + wsl * WSLOT + e * UB;
-                        if (e == 0 || two) {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const uint4 v = *reinterpret_cast<const uint4 *>(u + tile * 1024 + (4 * gi_ + c) * 32 + 16 * half);
-                                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                                for (int j2 = 0; j2 < 4; ++j2) {
-                                    av[e][8 * c + 2 * j2] = dec8_pair<0>(wv[j2]);
-                                    av[e][8 * c + 2 * j2 + 1] = dec8_pair<1>(wv[j2]);
-                                }
-                            }
-                            sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
-                        } else {
-#pragma unroll
-                            for (int m = 0; m < 32; ++m) av[e][m] = 0u;
-                        }
+    if (warp < DQ0) {
+        regs_dec<REGS_WG0>();
+        if (warp == 0) {
+            // ---------------- weight producer: units (k, k + 1) of a segment in
+            // one 1-D bulk copy (a row block's units are consecutive)
+            bool ok = true;
+            int jp = 0;                                   // weight stages used so far
+            for (long long u = lo; u < hi && ok;) {
+                const int tile = (int)(u / G), k0 = (int)(u % G);
+                const int k1 = (int)min((long long)G, k0 + (hi - u));
+                const WideTile tr = wide_tile(args, tile);
+                const int UB = unit_bytes(tr.P->codec);
+                const uint8_t *units = tr.P->packed + (size_t)tr.blk * G * UB;
+                for (int k = k0; k < k1; k += 2, ++jp) {
+                    const int wsl = jp % NWP;
+                    const uint32_t bytes = (k + 1 < k1 ? 2 : 1) * UB;
+                    if (jp >= NWP && !(ok = mbar_wait_warp(&w_empty[wsl], ((jp / NWP) - 1) & 1, args.status))) break;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&w_full[wsl], bytes);
+                        bulk_g2s(ws + wsl * WSLOT, units + (size_t)k * UB, bytes, &w_full[wsl]);
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&w_empty[wsl]);
-                } else {
-                uint32_t wd[2][8], hw[2][4];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint8_t *u = ws + wsl * WSLOT + e * UB;
-                    if (e == 0 || two) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi_ + c) * 16 + 8 * half);
-                            wd[e][2 * c] = v.x;
-                            wd[e][2 * c + 1] = v.y;
-                            hw[e][c] = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(u + NIB_BYTES + tile * 128 + (4 * gi_ + c) * 4) : 0u;
-                        }
-                        // the epilogue of step g0 + e reads this row's scale from the ring
-                        sc_ring[((g0 + e) % SC_RING) * BM + r] = __half2float(*reinterpret_cast<const __half *>(u + soff));
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) { wd[e][2 * c] = wd[e][2 * c + 1] = 0u; hw[e][c] = 0u; }
+                }
+                u += k1 - k0;
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
+        } else if (warp == 2) {
+            // ---------------- activation producer: 128B-swizzled X tiles, 2-D TMA
+            pdl_wait_prior();                             // X may belong to the previous kernel
+            if (lane == 0) pdl_launch_dependents();
+            bool ok = true;
+            int gi = 0;
+            for (long long u = lo; u < hi && ok;) {
+                const int tile = (int)(u / G), k0 = (int)(u % G);
+                const int k1 = (int)min((long long)G, k0 + (hi - u));
+                const WideTile tr = wide_tile(args, tile);
+                for (int k = k0; k < k1; ++k, ++gi) {
+                    const int s = gi % NS;
+                    if (gi >= NS && !(ok = mbar_wait_warp(&xa_empty[s], ((gi / NS) - 1) & 1, args.status))) break;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&xa_full[s], XST);
+                        tma_load_2d(xs + s * XST, &xmap, k * GROUP, tr.tt * BN, &xa_full[s]);
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[wsl]);
-                // decode to 32 bf16x2 words per group in natural k order: word m = (k 2m, 2m+1)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t w = wd[e][2 * c + h];
-                            uint32_t *o = av[e] + 8 * c + 4 * h;
-                            if (CODEC == 4) {
-                                o[0] = dec4_pair<0>(w); o[1] = dec4_pair<4>(w); o[2] = dec4_pair<8>(w); o[3] = dec4_pair<12>(w);
-                            } else {
-                                // this row's words in the lane's high word: m = 2*half + h
-                                const uint32_t hh = hw[e][c] >> (4 * (2 * half + h));   // bits 4m+p / 16+4m+p -> p / 16+p
-                                o[0] = dec5_pair<0, -4>(w, hh); o[1] = dec5_pair<4, -3>(w, hh);
-                                o[2] = dec5_pair<8, -2>(w, hh); o[3] = dec5_pair<12, -1>(w, hh);
-                            }
-                        }
-                    }
-                }
-                }
-                // the A stages of both groups are free once the MMAs of steps
-                // g0 - NA and g0 + 1 - NA have completed
-                const int h0 = g0 - NA, h1 = g0 + 1 - NA;
-                if (two && h1 >= 0 && h0 >= 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait2(&done[h0 % NS], (h0 / NS) & 1, &done[h1 % NS], (h1 / NS) & 1,
-                                                            args.status));
-                } else if (h0 >= 0) {
-                    ok = mbar_wait_warp(&done[h0 % NS], (h0 / NS) & 1, args.status);
-                } else if (two && h1 >= 0) {
-                    ok = mbar_wait_warp(&done[h1 % NS], (h1 / NS) & 1, args.status);
-                }
-                if (!ok) break;
+                u += k1 - k0;
+            }
+            if (!ok && lane == 0) *abort_flag = 1;
+        } else {
+            // ---------------- MMA issuers: warp 1 the even steps, warp 3 the odd
+            // ones (for H = 2: the first and the second half of every unit).
+            // Issuing a tensor-core instruction occupies the issuing warp's
+            // scheduler for tens of cycles; two issuers on two schedulers halve
+            // what the epilogue and dequant warps sharing them lose.
+            bool ok = true;
+            const int parity = warp >> 1;
+            const uint32_t idesc = idesc_bf16(BM, BH);
+            const int steps = (int)(hi - lo) * H;
+            int last = -1;
+            for (int j = parity; j < steps; j += 2) {
+                const int gi = j / H, h = j % H;
+                const int s = gi % NS, b = j % NP;
+                if (!(ok = mbar_wait_warp(&xa_full[s], (gi / NS) & 1, args.status))) break;
+                if (j >= NP && !(ok = mbar_wait_warp(&pfree[b], ((j / NP) - 1) & 1, args.status))) break;
                 tc_fence_after();
-                tc_st32(tmem + tlane + A_COL + (g0 % NA) * 32, av[0]);
-                if (two) tc_st32(tmem + tlane + A_COL + ((g0 + 1) % NA) * 32, av[1]);
-                tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&go[g0 % NS]);
-                    if (two) mbar_arrive(&go[(g0 + 1) % NS]);
+                const uint32_t d = tmem + P_COL + b * BH;
+                const uint32_t a = tmem + A_COL + (gi % NA) * 32;
+                const uint32_t b0 = smem_u32(xs + s * XST + h * HALF_BYTES);
+                // one elected lane per instruction: measured cheaper to issue
+                // than one elected block of four
+#pragma unroll
+                for (int kk = 0; kk < GROUP / 16; ++kk)
+                    if (elect_one()) tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
+                if (elect_one()) {
+                    tc_commit(&pfull[b]);
+                    tc_commit(&xa_empty[s]);
                 }
+                __syncwarp();
+                last = j;
+            }
+            if (!ok) {
+                if (lane == 0) *abort_flag = 1;
+                // let the MMAs this warp issued complete before tensor memory goes
+                if (last >= 0) mbar_wait_limit(&pfull[last % NP], (last / NP) & 1, args.status, 64);
             }
         }
+    } else if (warp < EPI0) {
+        // ---------------- dequant: thread = weight row of the tile
+        regs_dec<Regs<H>::DQ>();
+        const int q = warp & 3;                           // tensor-memory lane quarter
+        bool ok = true;
+        int gi = 0, jp = 0;
+        for (long long u = lo; u < hi && ok;) {
+            const int tile = (int)(u / G), k0 = (int)(u % G);
+            const int k1 = (int)min((long long)G, k0 + (hi - u));
+            const int codec = wide_tile(args, tile).P->codec;
+            if (F8 && codec == 8)
+                ok = dequant_segment<8, NS, NWP, WSLOT, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                                                        tmem, q, lane, args.status);
+            else if (codec == 5)
+                ok = dequant_segment<5, NS, NWP, WSLOT, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                                                        tmem, q, lane, args.status);
+            else
+                ok = dequant_segment<4, NS, NWP, WSLOT, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                                                        tmem, q, lane, args.status);
+            u += k1 - k0;
+        }
         if (!ok && lane == 0) *abort_flag = 1;
-    } else if (warp >= EPI0) {
-        // ---------------- epilogue: thread = row r, columns [64*hc, 64*hc + 64)
-        const int q = warp & 3, hc = (warp - EPI0) >> 2;
+    } else {
+        // ---------------- epilogue: thread = row r of the tile, tokens
+        // [64 c, 64 c + 64) of each 128-token half
+        regs_inc<Regs<H>::EPI>();
+        pdl_wait_prior();                                 // Y, R and the workspace follow the previous kernel
+        const int q = warp & 3, c = (warp - EPI0) >> 2, e = warp - EPI0;
         const int r = q * 32 + lane;
-        // the first NP steps find their P buffer empty
-        if (lane == 0)
-            for (int g = 0; g < NP && g < steps; ++g) mbar_arrive(&go[g]);
+        const uint32_t tl = (uint32_t)(q * 32) << 16;
         bool ok = true;
         int gi = 0;
-        for (int it = 0; it < my_tiles && ok; ++it) {
-            float2 acc[32];
+        for (long long u = lo; u < hi && ok;) {
+            const int tile = (int)(u / G), k0 = (int)(u % G);
+            const int k1 = (int)min((long long)G, k0 + (hi - u));
+            float2 acc[H][32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.f, 0.f);
-            for (int k = 0; k < G; ++k, ++gi) {
-                const int ps = gi % NP;
-                // polled: the epilogue gates the MMAs of step gi + NP
-                if (!(ok = mbar_spin_warp(&done[gi % NS], (gi / NS) & 1, args.status))) break;
-                tc_fence_after();
-                const float s = sc_ring[(gi % SC_RING) * BM + r];
-                const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + P_COL + ps * BN + hc * 64;
-                // both loads in flight before one wait: the P buffer is released
-                // one load latency after it filled
-                uint32_t v0[32], v1[32];
-                tc_ld32(base, v0);
-                tc_ld32(base + 32, v1);
-                tc_wait_ld();
-                tc_regs_ready(v0);
-                tc_regs_ready(v1);
-                tc_fence_before();
-                __syncwarp();
-                // P buffer ps is free for step gi + NP
-                if (lane == 0 && gi + NP < steps) mbar_arrive(&go[(gi + NP) % NS]);
-                // packed f32x2 FMAs: half the instructions of scalar ones
-                const float2 s2 = make_float2(s, s);
+            for (int h = 0; h < H; ++h)
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    acc[j] = ffma2(s2, make_float2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), acc[j]);
+                for (int j = 0; j < 32; ++j) acc[h][j] = make_float2(0.f, 0.f);
+            for (int k = k0; k < k1 && ok; ++k, ++gi) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    acc[16 + j] = ffma2(s2, make_float2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), acc[16 + j]);
-            }
-            if (!ok) break;
-            // ---- write this tile's Y[t][n] (consecutive lanes = consecutive rows
-            // n) while the MMAs of the next tile run
-            const WideTile tr = wide_tile(args, blockIdx.x + it * gridDim.x);
-            const int n = tr.blk * BM + r;
-            if constexpr (FUSED) {
-                wide_fused_out(*tr.P, n, tr.tt * BN + hc * 64, T, acc);
-            } else if (n < tr.P->N) {
-                float *Y = static_cast<float *>(tr.P->Y);
-                const int N = tr.P->ncols;
-                const int t0 = tr.tt * BN + hc * 64;
+                for (int h = 0; h < H; ++h) {
+                    const int j = gi * H + h;
+                    const int b = j % NP;
+                    // a suspending wait: with three P buffers the epilogue has
+                    // two steps of MMA time to drain one, and polling warps
+                    // would take the dequant warps' issue slots
+                    if (!(ok = mbar_wait_warp(&pfull[b], (j / NP) & 1, args.status))) break;
+                    tc_fence_after();
+                    // the unit's scale (stored by the dequant before the MMAs
+                    // of this step could start)
+                    const float sc = sc_ring[(gi % SC_RING) * BM + r];
+                    const float2 s2 = make_float2(sc, sc);
+                    const uint32_t base = tmem + tl + P_COL + b * BH + 64 * c;
+                    if constexpr (H == 1) {
+                        // both loads in flight before one wait: the buffer is
+                        // released one load latency after it filled
+                        uint32_t v0[32], v1[32];
+                        tc_ld32(base, v0);
+                        tc_ld32(base + 32, v1);
+                        tc_wait_ld();
+                        tc_regs_ready(v0);
+                        tc_regs_ready(v1);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&pfree[b]);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = t0 + 2 * j;
-                    if (t < T) Y[(size_t)t * N + n] = acc[j].x;
-                    if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[j].y;
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1])),
+                                              acc[h][i]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][16 + i] = ffma2(s2, make_float2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1])),
+                                                   acc[h][16 + i]);
+                    } else {
+                        // one 32-column load at a time (registers hold the 128
+                        // accumulators); three P buffers give the two round
+                        // trips two steps of MMA time
+                        uint32_t v[32];
+                        tc_ld32(base, v);
+                        tc_wait_ld();
+                        tc_regs_ready(v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                              acc[h][i]);
+                        tc_ld32(base + 32, v);
+                        tc_wait_ld();
+                        tc_regs_ready(v);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&pfree[b]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][16 + i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                                   acc[h][16 + i]);
+                    }
                 }
             }
+            if (!ok) break;
+            // ---- the segment is done: write the tile, or leave a partial sum
+            // (the MMAs of the next segment run meanwhile)
+            const WideTile tr = wide_tile(args, tile);
+            const int n = tr.blk * BM + r;
+            const int t0 = tr.tt * BN + 64 * c;
+            if (k0 == 0 && k1 == G) {
+                store_tile<H, FUSED>(*tr.P, n, t0, T, acc);
+            } else {
+                const long long u0 = (long long)tile * G;
+                const int c_first = range_cta(U, gridDim.x, u0), c_last = range_cta(U, gridDim.x, u0 + G - 1);
+                // a CTA's first segment goes to its slot 0, its last to slot 1
+                float *mine = args.part + (size_t)(blockIdx.x * 2 + (lo >= u0 ? 0 : 1)) * BN * BM;
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int t = h * BH + 64 * c + 2 * j;
+                        mine[(size_t)t * BM + r] = acc[h][j].x;
+                        mine[(size_t)(t + 1) * BM + r] = acc[h][j].y;
+                    }
+                __threadfence();
+                __syncwarp();
+                unsigned int *cnt = tr.P->cnt + (size_t)tr.local * EPI_WARPS + e;
+                unsigned int old = 0;
+                if (lane == 0) old = atomicAdd(cnt, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == (unsigned int)(c_last - c_first)) {
+                    // the last of the tile's segments sums them all
+                    __threadfence();
+                    fixup_sum<H, BN>(acc, args.part, U, (int)gridDim.x, c_first, c_last, u0, c, r);
+                    if (lane == 0) *cnt = 0;              // zero again for the next run
+                    store_tile<H, FUSED>(*tr.P, n, t0, T, acc);
+                }
+            }
+            u += k1 - k0;
         }
         if (!ok && lane == 0) *abort_flag = 1;
     }
@@ -544,9 +752,10 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag) {
-        // a wait gave up: copies and MMAs already issued finish within
-        // microseconds; give them a bounded pause before the memory they
-        // write is released
+        // a wait gave up: the MMA warps have waited (bounded) for their own
+        // MMAs; bulk and TMA copies already issued move at most 32 KB each and
+        // land within microseconds even on a loaded GPU, so a 200 us pause
+        // bounds them before the memory they write is released
         for (int i = 0; i < 200; ++i) __nanosleep(1000);
         __syncthreads();
     }
@@ -576,14 +785,14 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map of X [T][K] bf16 with {64 columns x 128 rows} boxes, 128B swizzle,
-// zero fill beyond T.
-static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K) {
+// Tensor map of X [T][K] bf16 with {64 columns x BN rows} boxes, 128B
+// swizzle, zero fill beyond T.
+static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K, int BN) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {GROUP, wide::BN};
+    const cuuint32_t box[2] = {GROUP, (cuuint32_t)BN};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -591,76 +800,105 @@ static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int wide_tile_tokens() { return wide::BN; }
+// Units (tile, group) per CTA below which a launch uses fewer CTAs: a CTA
+// with a handful of groups spends more on its pipeline fill and partial sum
+// than it saves.
+constexpr int MIN_UNITS_PER_CTA = 8;
 
-template <int CODEC, bool FUSED>
-static cudaError_t launch_codec(const WideParent *parents, int np, const CUtensorMap &xmap, int T, int K,
-                                unsigned int *status, cudaStream_t stream) {
+int wide_tile_tokens(int halves) { return halves * wide::BH; }
+
+// Workspace of the wide route for a plan of `rows` packed rows and widths up
+// to T_max: the partial-sum slots of one launch (two per CTA, sized for the
+// widest tile the plan can take) and the plan's split-tile counters (eight
+// per tile at the plan's largest tile count).
+size_t wide_workspace_bytes(int rows, int T_max, int sms) {
+    if (T_max <= 32) return 0;
+    const int NB = (rows + wide::BM - 1) / wide::BM;
+    const int halves = T_max > wide::BH ? 2 : 1;
+    const size_t part = (size_t)sms * 2 * halves * wide::BH * wide::BM * sizeof(float);
+    const size_t tiles = (size_t)NB * ((T_max + wide::BH - 1) / wide::BH);   // at least the tiles of either width
+    return part + tiles * wide::EPI_WARPS * sizeof(unsigned int);
+}
+
+size_t wide_partial_bytes(int T_max, int sms) {
+    const int halves = T_max > wide::BH ? 2 : 1;
+    return (size_t)sms * 2 * halves * wide::BH * wide::BM * sizeof(float);
+}
+
+template <int H, bool FUSED, bool F8>
+static cudaError_t launch_t(const WideArgs &a, const CUtensorMap &xmap, int grid, bool pdl, cudaStream_t stream) {
     static std::atomic<bool> attr_set[64];
-    static std::atomic<int> sms[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(wide_kernel<CODEC, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 wide::Smem::BYTES);
+        e = cudaFuncSetAttribute(wide_kernel<H, FUSED, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 wide::Geo<H, F8>::BYTES);
         if (e != cudaSuccess) return e;
-        int n = 0;
-        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        sms[dev].store(n, std::memory_order_relaxed);
         attr_set[dev].store(true, std::memory_order_release);
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(wide::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = wide::Geo<H, F8>::BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, wide_kernel<H, FUSED, F8>, a, xmap);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int H>
+static cudaError_t launch_h(const WideArgs &a, const CUtensorMap &xmap, int grid, bool fused, bool f8, bool pdl,
+                            cudaStream_t stream) {
+    if (f8) return fused ? launch_t<H, true, true>(a, xmap, grid, pdl, stream)
+                         : launch_t<H, false, true>(a, xmap, grid, pdl, stream);
+    return fused ? launch_t<H, true, false>(a, xmap, grid, pdl, stream)
+                 : launch_t<H, false, false>(a, xmap, grid, pdl, stream);
+}
+
+// All parents (any mix of codecs) over one shared X in one launch of 128-token
+// (halves = 1) or 256-token (halves = 2) tiles.  part: the partial-sum slots
+// (wide_partial_bytes for this width); each parent's cnt its zeroed counters.
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int halves, float *part,
+                        unsigned int *status, bool pdl, int sms, cudaStream_t stream) {
+    const int BN = halves * wide::BH;
+    CUtensorMap xmap;
+    cudaError_t e = make_xmap(&xmap, X, T, K, BN);
+    if (e != cudaSuccess) return e;
     WideArgs a;
     memset(&a, 0, sizeof a);
-    const int ntt = (T + wide::BN - 1) / wide::BN;
+    const int ntt = (T + BN - 1) / BN;
     int tiles = 0;
+    bool fused = false, f8 = false;
     for (int i = 0; i < np; ++i) {
-        if (parents[i].codec != CODEC) continue;
         WideParent &d = a.p[a.nparents++];
         d = parents[i];
         d.cta_begin = tiles;
         d.nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
         tiles += d.nblocks * ntt;
+        fused = fused || parents[i].epi != EPI_STORE || parents[i].ybf16;
+        f8 = f8 || parents[i].codec == 8;
     }
-    if (tiles == 0) return cudaSuccess;
     a.T = T;
     a.K = K;
     a.G = K / GROUP;
     a.ntt = ntt;
     a.ntiles = tiles;
+    a.units = (long long)tiles * a.G;
+    a.part = part;
     a.status = status;
-    // persistent: one CTA per SM (its shared memory allows no more), each
-    // taking the tiles blockIdx.x, blockIdx.x + grid, ...
-    const int nsm = sms[dev].load(std::memory_order_relaxed);
-    const int grid = tiles < nsm ? tiles : nsm;
-    wide_kernel<CODEC, FUSED><<<grid, wide::THREADS, wide::Smem::BYTES, stream>>>(a, xmap);
-    return cudaGetLastError();
-}
-
-// Parents of both codecs in one call become one launch per codec.
-cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, unsigned int *status,
-                        cudaStream_t stream, int *launches) {
-    CUtensorMap xmap;
-    cudaError_t e = make_xmap(&xmap, X, T, K);
-    if (e != cudaSuccess) return e;
-    int n4 = 0, n5 = 0, n8 = 0;
-    bool fused = false;
-    for (int i = 0; i < np; ++i) {
-        (parents[i].codec == 4 ? n4 : parents[i].codec == 5 ? n5 : n8)++;
-        fused = fused || parents[i].epi != EPI_STORE || parents[i].ybf16;
-    }
-    if (n4 && (e = fused ? launch_codec<4, true>(parents, np, xmap, T, K, status, stream)
-                         : launch_codec<4, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
-        return e;
-    if (n5 && (e = fused ? launch_codec<5, true>(parents, np, xmap, T, K, status, stream)
-                         : launch_codec<5, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
-        return e;
-    if (n8 && (e = fused ? launch_codec<8, true>(parents, np, xmap, T, K, status, stream)
-                         : launch_codec<8, false>(parents, np, xmap, T, K, status, stream)) != cudaSuccess)
-        return e;
-    *launches = (n4 > 0) + (n5 > 0) + (n8 > 0);
-    return cudaSuccess;
+    // one CTA per SM (the shared memory allows no more), each with an equal
+    // share of the units
+    long long grid = a.units / MIN_UNITS_PER_CTA;
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    return halves == 2 ? launch_h<2>(a, xmap, (int)grid, fused, f8, pdl, stream)
+                       : launch_h<1>(a, xmap, (int)grid, fused, f8, pdl, stream);
 }
 
 }  // namespace qg

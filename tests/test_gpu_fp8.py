@@ -83,13 +83,17 @@ def test_repeatable(T):
 
 @pytest.mark.parametrize("T", [4, 16, 64])
 def test_multi_parent_with_int4(T):
-    # at T = 64 (tcgen05) the two codecs take one launch each
+    # every route serves both codecs in one launch (at T = 64 the tcgen05
+    # route resolves the codec per tile)
     K = 5120
     pf = synth.weights(64, 4096, K, 8, parent=0)
     pi = synth.weights(64, 1024, K, 4, parent=1)
     ws = [weights(pf, T_max=64), weights(pi, T_max=64)]
     x = synth.activations(64, T, K, outliers=True)
-    Ys = qg.run_multi(ws, dev_x(x))
+    X = dev_x(x)
+    n0 = qg.qgemm_launch_count()
+    Ys = qg.run_multi(ws, X)
+    assert qg.qgemm_launch_count() - n0 == 1
     for p, Y in zip((pf, pi), Ys):
         Yref, A = oracle.gemm_parent(p, x)
         assert_close(host(Y), Yref, A, f"multi int{p['bits']} T={T}")

@@ -179,7 +179,8 @@ def test_one_route_per_call(T):
     W.run(X)
     launched = qg.qgemm_launch_count() - n0
     assert launched == 1, (route, launched)
-    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "skinny32" if T <= 32 else "tcgen05_128x128")
+    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "skinny32" if T <= 32
+                     else "tcgen05_128x128" if T <= 128 else "tcgen05_128x256")
     n0 = qg.qgemm_launch_count()
     qg.GroupwiseWeights(4, 256, 512, p["packed"], p["scales"], T_max=8)
     assert qg.qgemm_launch_count() - n0 == 2            # pack + its ordering kernel

@@ -47,6 +47,7 @@ EXPORTS = [
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
     "qgemm_device_status", "qgemm_plan_set_pdl", "qgemm_pair_packed_bytes", "qgemm_pack_pair",
     "qgemm_plan_set_epilogue", "qgemm_run_ex", "qgemm_selftest_timeout", "qgemm_plan_force_route",
+    "qgemm_run_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -83,6 +84,7 @@ def _declare(lib):
         "qgemm_run_ex": ([vp, vp, i32, vp, vp, vp], i32),
         "qgemm_selftest_timeout": ([vp], i32),
         "qgemm_plan_force_route": ([vp, i32], i32),
+        "qgemm_run_noalloc": ([vp, vp, vp, i32, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -164,6 +166,12 @@ def qgemm_run_multi(plans, X, T: int, Ys, stream=None) -> int:
     parr = (ctypes.c_void_p * max(n, 1))(*plans)
     yarr = (ctypes.c_void_p * max(len(Ys), 1))(*[_ptr(y) for y in Ys])
     return load().qgemm_run_multi(parr, n, _ptr(X), T, yarr, _stream(stream))
+
+
+def qgemm_run_noalloc(plan, packed_dev, X, T: int, Y, stream=None) -> int:
+    """qgemm_run on the tcgen05 route with the library's own scratch array, for
+    callers that cannot allocate device memory (see include/qgemm.h)."""
+    return load().qgemm_run_noalloc(plan, _ptr(packed_dev), _ptr(X), T, _ptr(Y), _stream(stream))
 
 
 def qgemm_plan_destroy(plan) -> int:

@@ -432,3 +432,80 @@ extern "C" qgemm_status qgemm_run_multi(const qgemm_plan_t *plans, int n_parents
     }
     return run_parents(ps, n_parents, X, T, ys, nullptr, (cudaStream_t)stream);
 }
+
+// ---------------------------------------------------------------- allocation-free runs
+//
+// Some callers cannot allocate device memory when they run a projection: an
+// engine that has reserved the GPU's memory up front under its own allocator,
+// a plugin loaded into a host whose memory budget is fixed, or code that must
+// not call cudaMalloc while other streams are being captured into CUDA graphs
+// (an allocation there synchronises the device or is refused).  Such callers
+// cannot provide the workspace that the tcgen05 route keeps its split tiles'
+// partial sums in.  qgemm_run_noalloc runs that route with a scratch array
+// the library owns instead: a file-scope device array of fixed size, which
+// every GPU that loads the library holds until the process exits.
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)32 << 20;   // the whole array
+constexpr size_t NOALLOC_COUNTER_BYTES = (size_t)256 << 10;  // of it, the split-tile counters
+constexpr size_t NOALLOC_MAX_TILES = NOALLOC_COUNTER_BYTES / (8 * sizeof(unsigned int));
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device, looked up on the
+// first call on each device (the host-side name of a __device__ array is not a
+// device address).
+static uint8_t *noalloc_scratch_ptr() {
+    constexpr int MAX_DEVICES = 64;
+    static std::atomic<uint8_t *> cache[MAX_DEVICES];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    uint8_t *p = cache[dev].load();
+    if (p) return p;
+    uint8_t *ptr = nullptr;
+    if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    cache[dev].store(ptr);
+    return ptr;
+}
+
+extern "C" qgemm_status qgemm_run_noalloc(qgemm_plan_t plan, const void *packed_dev, const void *X, int T, float *Y,
+                                          qgemm_stream_t stream) {
+    if (!plan || !plain_output(plan) || !packed_dev || T < 0) return QGEMM_ERR_INVALID_ARG;
+    if (T > plan->T_max) return QGEMM_ERR_T_OUT_OF_DOMAIN;
+    if (T == 0) return QGEMM_OK;
+    if (!X || !Y) return QGEMM_ERR_INVALID_ARG;
+    if (!aligned16(packed_dev) || !aligned16(X) || !aligned16(Y)) return QGEMM_ERR_ALIGNMENT;
+    const int halves = T > 128 ? 2 : 1;
+    const int BN = 128 * halves;
+    const size_t tiles = (size_t)plan->NB * (size_t)((T + BN - 1) / BN);
+    if (tiles > NOALLOC_MAX_TILES) return QGEMM_ERR_WORKSPACE;   // more tiles than the counters cover
+    uint8_t *scratch = noalloc_scratch_ptr();
+    unsigned int *status = status_ptr();
+    if (!scratch || !status) return QGEMM_ERR_CUDA;
+    // the counters start at zero on every call (a run that gave up leaves
+    // some behind); the partial sums need no clearing
+    if (cudaMemsetAsync(scratch, 0, tiles * 8 * sizeof(unsigned int), (cudaStream_t)stream) != cudaSuccess)
+        return QGEMM_ERR_CUDA;
+    // as many CTAs as the partial-sum slots (two per CTA) fit
+    const size_t slot_pair = (size_t)2 * BN * 128 * sizeof(float);
+    const int fit = (int)((NOALLOC_SCRATCH_BYTES - NOALLOC_COUNTER_BYTES) / slot_pair);
+    WideParent wp;
+    memset(&wp, 0, sizeof wp);
+    wp.packed = static_cast<const uint8_t *>(packed_dev);
+    wp.Y = Y;
+    wp.cnt = reinterpret_cast<unsigned int *>(scratch);
+    wp.N = plan->rows;
+    wp.codec = plan->codec;
+    wp.ncols = plan->N;
+    wp.epi = plan->epi;
+    if (launch_wide(&wp, 1, X, T, plan->K, halves, reinterpret_cast<float *>(scratch + NOALLOC_COUNTER_BYTES), status,
+                    false, plan->sms < fit ? plan->sms : fit, (cudaStream_t)stream) != cudaSuccess)
+        return QGEMM_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return QGEMM_OK;
+}

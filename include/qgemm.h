@@ -311,6 +311,40 @@ qgemm_status qgemm_device_status(qgemm_stream_t stream, int clear);
  */
 qgemm_status qgemm_selftest_timeout(qgemm_stream_t stream);
 
+/*
+ * ---------------------------------------------------------- allocation-free run
+ *
+ * Y[T][N] = X[T][K] . deq(W)^T like qgemm_run, on the tcgen05 route at every
+ * T, for callers that cannot allocate device memory when they run: an engine
+ * that has reserved the GPU's memory up front for its own allocator, a plugin
+ * in a host with a fixed memory budget, code that must not call cudaMalloc
+ * while streams are being captured.  They cannot supply the workspace that
+ * route keeps its split tiles' partial sums in (qgemm_plan_bind), so this call
+ * uses a scratch array inside the library: 32 MiB of device memory that every
+ * GPU which loads the library holds until the process exits (256 KiB of it
+ * counts the tiles whose groups several CTAs share, the rest holds their
+ * partial sums).  The call allocates nothing itself.
+ *   plan        from qgemm_plan (default output, STORE / F32); it need not be
+ *               bound -- the weights come from packed_dev
+ *   packed_dev  the matrix packed by qgemm_pack_weights for this plan's N, K
+ *               and codec, 16-byte aligned
+ *   X, Y        as qgemm_run
+ * The scratch array is looked up on the first call on each device (make that
+ * first call before any stream capture on the device).  Every call clears the
+ * array's counters at its start on `stream` (one memset) and uses as many
+ * CTAs as its partial-sum slots fit (up to the SM count for 128-token tiles,
+ * T <= 128; 127 for 256-token tiles).  All calls on a device share the array,
+ * so calls that overlap on the GPU (other streams, other host threads)
+ * corrupt each other's results: order them on one stream.
+ * No passage of the pages corresponds to this call; it is a deployment
+ * convenience of the library.
+ * Errors: as qgemm_run (a NULL packed_dev is QGEMM_ERR_INVALID_ARG), and
+ * QGEMM_ERR_WORKSPACE when ceil(N / 128) * ceil(T / BN) tiles (BN = 128 for
+ * T <= 128, else 256) exceed the 8,192 the counters cover.
+ */
+qgemm_status qgemm_run_noalloc(qgemm_plan_t plan, const void *packed_dev, const void *X, int T, float *Y,
+                               qgemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,8 +20,8 @@ cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pd
 int skinny_line_groups(int G, int nj_pref);
 cudaError_t launch_skinny_line(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, bool f8,
                                cudaStream_t stream);
-cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int halves, float *part,
-                        unsigned int *status, bool pdl, int sms, cudaStream_t stream);
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int bh, int halves,
+                        float *part, unsigned int *status, bool pdl, int sms, cudaStream_t stream);
 size_t wide_workspace_bytes(int rows, int T_max, int sms);
 size_t wide_partial_bytes(int T_max, int sms);
 }  // namespace qg
@@ -36,33 +36,41 @@ enum Route : int {
     ROUTE_SKINNY32 = 2,    // 32-token tile
     ROUTE_WIDE128 = 3,     // stream-K tcgen05 tiles of 128 rows x 128 tokens
     ROUTE_WIDE256 = 4,     // stream-K tcgen05 tiles of 128 rows x 256 tokens (two 128-token halves)
+    ROUTE_WIDE64 = 5,      // stream-K tcgen05 tiles of 128 rows x 64 tokens (six P buffers)
     ROUTE_COUNT
 };
 
 static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "tcgen05_128x128",
-                                               "tcgen05_128x256"};
+                                               "tcgen05_128x256", "tcgen05_128x64"};
 
 static int route_tokens(int route) {
     switch (route) {
         case ROUTE_SKINNY8: return 8;
         case ROUTE_SKINNY16: return 16;
         case ROUTE_SKINNY32: return 32;
+        case ROUTE_WIDE64: return 64;
         case ROUTE_WIDE128: return 128;
         default: return 256;
     }
 }
 
-static bool wide_route(int route) { return route == ROUTE_WIDE128 || route == ROUTE_WIDE256; }
+static bool wide_route(int route) { return route == ROUTE_WIDE64 || route == ROUTE_WIDE128 || route == ROUTE_WIDE256; }
 
-// Narrowest tile that covers T (the padded width sets the cost, not the live
-// column count).  A route forced on the plan (qgemm_plan_force_route) takes
-// every T its token tile covers.
-static int table_route(int T) {
+// The route table, from per-T sweeps with every route forced on the pages'
+// projection shapes (5120 x 6144, 7168 x 5120, 12288 x 5120; cold weights):
+// the narrowest tile that covers T (the padded width sets the cost, not the
+// live column count), except that the 64-token tcgen05 tile beats the
+// 32-token small-T tile from T = 17 on, and that above 128 tokens the
+// 256-token tile pays only from 512 tokens, or from 129 when the launch has
+// at least 96 row blocks of 128 (enough tiles to fill the GPU either way).
+// nb: the launch's 128-row blocks, summed over its parents.  A route forced
+// on the plan (qgemm_plan_force_route) takes every T its token tile covers.
+static int table_route(int T, int nb) {
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
-    if (T <= 32) return ROUTE_SKINNY32;
+    if (T <= 64) return ROUTE_WIDE64;
     if (T <= 128) return ROUTE_WIDE128;
-    return ROUTE_WIDE256;
+    return (T >= 512 || nb >= 96) ? ROUTE_WIDE256 : ROUTE_WIDE128;
 }
 
 // the tcgen05 routes walk any number of token tiles
@@ -83,8 +91,8 @@ struct qgemm_plan_s {
     bool bound;
 };
 
-static int choose_route(const qgemm_plan_s *p, int T) {
-    return (p->forced_route >= 0 && route_covers(p->forced_route, T)) ? p->forced_route : table_route(T);
+static int choose_route(const qgemm_plan_s *p, int T, int nb) {
+    return (p->forced_route >= 0 && route_covers(p->forced_route, T)) ? p->forced_route : table_route(T, nb);
 }
 
 static std::atomic<uint64_t> g_launches{0};
@@ -253,7 +261,7 @@ qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable) {
 
 int qgemm_plan_route(qgemm_plan_t plan, int T) {
     if (!plan || T < 1 || T > plan->T_max) return -1;
-    return choose_route(plan, T);
+    return choose_route(plan, T, plan->NB);
 }
 
 // Whether the plan's workspace holds what `route` needs: the tcgen05 routes
@@ -261,7 +269,7 @@ int qgemm_plan_route(qgemm_plan_t plan, int T) {
 // 256-token tiles above 128).
 static bool workspace_fits(const qgemm_plan_s *p, int route) {
     if (!wide_route(route)) return true;
-    return p->T_max > 32 && (route == ROUTE_WIDE128 || p->T_max > 128);
+    return p->T_max > 32 && (route != ROUTE_WIDE256 || p->T_max > 128);
 }
 
 qgemm_status qgemm_plan_force_route(qgemm_plan_t plan, int route) {
@@ -320,8 +328,11 @@ static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, void *Y, const 
 // One or more parents over the same X in one launch of the route T selects.
 static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const void *X, int T,
                                 void *const *Ys, const float *R, cudaStream_t stream) {
-    // parents of one launch share its route: the first plan's choice
-    const int route = choose_route(plans[0], T);
+    // parents of one launch share its route: the first plan's choice for the
+    // launch's row blocks
+    int nb = 0;
+    for (int i = 0; i < np; ++i) nb += plans[i]->NB;
+    const int route = choose_route(plans[0], T, nb);
     const int K = plans[0]->K;
     const int G = K / GROUP;
     unsigned int *status = status_ptr();
@@ -345,8 +356,8 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
             wp[i].ybf16 = plans[i]->out == QGEMM_OUT_BF16;
         }
         // the partial-sum slots of the first parent's workspace serve the launch
-        if (launch_wide(wp, np, X, T, K, route == ROUTE_WIDE256 ? 2 : 1, reinterpret_cast<float *>(plans[0]->ws),
-                        status, pdl, plans[0]->sms, stream) != cudaSuccess)
+        if (launch_wide(wp, np, X, T, K, route == ROUTE_WIDE64 ? 64 : 128, route == ROUTE_WIDE256 ? 2 : 1,
+                        reinterpret_cast<float *>(plans[0]->ws), status, pdl, plans[0]->sms, stream) != cudaSuccess)
             return QGEMM_ERR_CUDA;
         g_launches.fetch_add(1);
         return QGEMM_OK;
@@ -503,8 +514,8 @@ extern "C" qgemm_status qgemm_run_noalloc(qgemm_plan_t plan, const void *packed_
     wp.codec = plan->codec;
     wp.ncols = plan->N;
     wp.epi = plan->epi;
-    if (launch_wide(&wp, 1, X, T, plan->K, halves, reinterpret_cast<float *>(scratch + NOALLOC_COUNTER_BYTES), status,
-                    false, plan->sms < fit ? plan->sms : fit, (cudaStream_t)stream) != cudaSuccess)
+    if (launch_wide(&wp, 1, X, T, plan->K, 128, halves, reinterpret_cast<float *>(scratch + NOALLOC_COUNTER_BYTES),
+                    status, false, plan->sms < fit ? plan->sms : fit, (cudaStream_t)stream) != cudaSuccess)
         return QGEMM_ERR_CUDA;
     g_launches.fetch_add(1);
     return QGEMM_OK;

@@ -61,31 +61,32 @@ namespace qg {
 namespace wide {
 
 constexpr int BM = 128;                   // weight rows per tile (tensor-memory lanes)
-constexpr int BH = 128;                   // tokens per MMA: one half of a 256-token tile
 constexpr int NA = 4;                     // A stages in tensor memory (unit u uses u mod NA)
-constexpr int NP = 3;                     // P buffers in tensor memory (step j uses j mod NP)
 constexpr int DQ_WARPS = 4;               // one dequant warp per tensor-memory lane quarter
 constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
 constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
 constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
 constexpr int SC_RING = 16;               // units of scales in flight
-constexpr int P_COL = 0;                  // P buffers: columns [0, 128 NP)
-constexpr int A_COL = NP * BH;            // A stages: columns [128 NP, 128 NP + 32 NA)
+constexpr int P_COL = 0;                  // P buffers from column 0, then the A stages
 constexpr int TMEM_COLS = 512;
-static_assert(A_COL + 32 * NA <= TMEM_COLS, "tensor memory budget");
 constexpr int X_REGION = 128 * 1024;      // activation stages
-constexpr int HALF_BYTES = BH * GROUP * 2;   // 16 KB: one half's X tile of one group
-// the dequant stores the scale of unit u + 1 once the MMAs of unit u - 1 - NA
-// are done, and those waited for the epilogue of three steps earlier
-static_assert(SC_RING >= NA + NP + 3, "scale ring shorter than the dequant lead");
 
-// H: halves per tile (BN = 128 H tokens); F8: a parent of the launch holds
-// FP8 codes (larger units, so fewer weight stages fit).
-template <int H, bool F8>
+// BH: tokens per MMA (64 or 128); H: MMAs ("halves") per tile, so BN = BH H
+// tokens; F8: a parent of the launch holds FP8 codes (larger units, so fewer
+// weight stages fit).  Tensor memory holds the A stages and as many P buffers
+// of BH columns as fit beside them: 3 of 128 columns or 6 of 64, so that the
+// epilogue has NP - 1 steps of MMA time to drain a buffer.
+template <int BH_, int H, bool F8>
 struct Geo {
+    static constexpr int BH = BH_;
+    static constexpr int NP = (TMEM_COLS - 32 * NA) / BH;  // P buffers (step j uses j mod NP)
+    static constexpr int A_COL = P_COL + NP * BH;         // A stages: 32 columns each
+    static constexpr int EW = BH / 2;                     // P columns per epilogue warp
+    static constexpr int NJ = EW / 2;                     // column pairs per epilogue thread and MMA
+    static constexpr int HALF_BYTES = BH * GROUP * 2;     // one MMA's X tile of one group
     static constexpr int BN = H * BH;
     static constexpr int XST = H * HALF_BYTES;           // X stage: BN tokens x 64 columns
-    static constexpr int NS = X_REGION / XST;             // 8 stages (H = 1) or 4 (H = 2)
+    static constexpr int NS = X_REGION / XST;             // 16, 8 or 4 stages
     static constexpr int WSLOT = 2 * (F8 ? UNIT8 : UNIT5);
     static constexpr int NWP = F8 ? 4 : 6;                // weight stages (pairs of units)
     static constexpr int X_OFF = 0;                       // 1024-aligned (128B swizzle atoms)
@@ -97,6 +98,11 @@ struct Geo {
     static constexpr int BYTES = MISC_OFF + 16 + 1024;    // + slack to align the base
     static_assert(NS >= NA, "A stages are recycled through the X stage barriers");
     static_assert(BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(A_COL + 32 * NA <= TMEM_COLS, "tensor memory budget");
+    // the dequant stores the scale of unit u + 1 once the MMAs of unit u - 1 -
+    // NA are done, and those waited for the epilogue of NP steps earlier
+    static_assert(SC_RING >= NA + NP + 2, "scale ring shorter than the dequant lead");
+    static_assert(BH == 64 || BH == 128, "MMA widths of the route");
 };
 
 }  // namespace wide
@@ -232,18 +238,29 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // accumulators per thread and reads a split tile's partials beside them, so
 // the producer, MMA and dequant warps give registers up for it.  The block
 // launches with 512 threads x 128 registers (65,536); the shares below add up
-// to 128 x (40 + 128) + 256 x 168 or 128 x (40 + 96) + 256 x 184 = 64,512.
+// to at most 64,512 for every tile shape: 128 x (40 + 136) + 256 x 160
+// (128-token tiles), 128 x (40 + 96) + 256 x 184 (256), 128 x (40 + 144) +
+// 256 x 152 (64).
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 template <int N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+constexpr int REGS_AT_LAUNCH = 128;
+// A warpgroup's register count from the launch's 128 to N: .dec may only
+// lower the count and .inc only raise it.
+template <int N>
+__device__ __forceinline__ void regs_set() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+    if constexpr (N < REGS_AT_LAUNCH) regs_dec<N>();
+    else if constexpr (N > REGS_AT_LAUNCH) regs_inc<N>();
+}
 // The 128-token tile's dequant decodes a pair of units at once (more
 // registers); the 256-token tile's epilogue holds twice the accumulators.
-constexpr int REGS_LAUNCH = 128, REGS_WG0 = 40;
-template <int H> struct Regs {
-    static constexpr int DQ = H == 1 ? 128 : 96;
-    static constexpr int EPI = H == 1 ? 168 : 184;
-    static_assert(128 * (REGS_WG0 + DQ) + 256 * EPI <= 512 * REGS_LAUNCH, "register split");
+template <int BH, int H> struct Regs {
+    static constexpr int WG0 = 40;
+    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 96;
+    static constexpr int EPI = BH == 64 ? 152 : H == 1 ? 160 : 184;
+    static_assert(128 * (WG0 + DQ) + 256 * EPI <= 512 * REGS_AT_LAUNCH, "register split");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -297,7 +314,7 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 // two units (the integer codecs on the 128-token tile, where a unit's MMAs
 // are short); otherwise one unit at a time (fewer live registers: the FP8
 // decode, the 256-token tile's accumulators).
-template <int CODEC, int NS, int NWP, int WSLOT, bool PAIR>
+template <int CODEC, int NS, int NWP, int WSLOT, int A_COL, bool PAIR>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
                                                 float *sc_ring, uint32_t tmem, int q, int lane,
@@ -368,12 +385,13 @@ __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp
 // A tile's fused outputs for one thread's 64 tokens t0 .. t0 + 63 of row n
 // (acc[j] = tokens t0 + 2j, t0 + 2j + 1): residual add, bf16, or SwiGLU,
 // where lanes l and l + 8 hold the gate and the up row of one output.
-__device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t0, int T, const float2 (&acc)[32]) {
+template <int NJ>
+__device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t0, int T, const float2 (&acc)[NJ]) {
     if (P.epi == EPI_SWIGLU) {
         const int f = (n >> 4) * 8 + (n & 7);
         const bool gate = (n & 8) == 0 && f < P.ncols;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             const float ux = __shfl_down_sync(0xffffffffu, acc[j].x, 8);
             const float uy = __shfl_down_sync(0xffffffffu, acc[j].y, 8);
             const int t = t0 + 2 * j;
@@ -386,7 +404,7 @@ __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t
         // so the compiler cannot move a load above an earlier store; every
         // element is read before it is written either way)
 #pragma unroll
-        for (int jb = 0; jb < 32; jb += 4) {
+        for (int jb = 0; jb < NJ; jb += 4) {
             float rv[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -403,7 +421,7 @@ __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t
         }
     } else if (n < P.N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < NJ; ++j) {
             const int t = t0 + 2 * j;
             if (t < T) epi_out(P, t, n, acc[j].x);
             if (t + 1 < T) epi_out(P, t + 1, n, acc[j].y);
@@ -411,20 +429,20 @@ __device__ __forceinline__ void wide_fused_out(const WideParent &P, int n, int t
     }
 }
 
-// Write one thread's finished accumulators: row n, tokens t0 + 128 h + 64 c
-// + 2j (+1) for each half h.
-template <int H, bool FUSED>
-__device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, int T, const float2 (&acc)[H][32]) {
+// Write one thread's finished accumulators: row n, tokens t0 + BH h + 2j
+// (+1) for each half h (t0 includes the thread's column block).
+template <int BH, int H, int NJ, bool FUSED>
+__device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, int T, const float2 (&acc)[H][NJ]) {
 #pragma unroll
     for (int h = 0; h < H; ++h) {
-        const int th = t0 + h * wide::BH;
+        const int th = t0 + h * BH;
         if constexpr (FUSED) {
             wide_fused_out(P, n, th, T, acc[h]);
         } else if (n < P.N) {
             float *Y = static_cast<float *>(P.Y);
             const int N = P.ncols;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < NJ; ++j) {
                 const int t = th + 2 * j;
                 if (t < T) Y[(size_t)t * N + n] = acc[h][j].x;
                 if (t + 1 < T) Y[(size_t)(t + 1) * N + n] = acc[h][j].y;
@@ -439,19 +457,19 @@ __device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, i
 // segments' CTAs c_first .. c_last in ascending order, so the order does not
 // depend on which CTA finishes last.  acc is overwritten (its registers hold
 // the running sum, 32 column pairs of one segment in flight beside it).
-template <int H, int BN>
-__device__ __forceinline__ void fixup_sum(float2 (&acc)[H][32], const float *part, long long U, int grid,
+template <int BH, int H, int NJ, int BN>
+__device__ __forceinline__ void fixup_sum(float2 (&acc)[H][NJ], const float *part, long long U, int grid,
                                           int c_first, int c_last, long long u0, int c, int r) {
-    constexpr int BM = wide::BM, BH = wide::BH;
-    constexpr int CH = H == 1 ? 32 : 16;              // column pairs in flight (registers)
+    constexpr int BM = wide::BM, EW = 2 * NJ;
+    constexpr int CH = H == 1 ? NJ : 16;              // column pairs in flight (registers)
 #pragma unroll
     for (int h = 0; h < H; ++h)
 #pragma unroll
-        for (int jb = 0; jb < 32; jb += CH) {
+        for (int jb = 0; jb < NJ; jb += CH) {
             // a CTA's first segment sits in its slot 0, its last in slot 1
             auto seg = [&](int cc) {
                 return part + (size_t)(cc * 2 + (range_lo(U, grid, cc) >= u0 ? 0 : 1)) * BN * BM +
-                       (size_t)(h * BH + 64 * c + 2 * jb) * BM + r;
+                       (size_t)(h * BH + EW * c + 2 * jb) * BM + r;
             };
             const float *p0 = seg(c_first);
 #pragma unroll
@@ -478,12 +496,13 @@ __device__ __forceinline__ void fixup_sum(float2 (&acc)[H][32], const float *par
 // every launch measured 12% slower at T = 4096).  F8: a parent holds FP8
 // codes.  Parents of different codecs share one launch: the codec is
 // resolved per tile.
-template <int H, bool FUSED, bool F8>
+template <int BH, int H, bool FUSED, bool F8>
 __global__ void __launch_bounds__(wide::THREADS, 1)
     wide_kernel(const __grid_constant__ WideArgs args, const __grid_constant__ CUtensorMap xmap) {
     using namespace wide;
-    using Gm = Geo<H, F8>;
+    using Gm = Geo<BH, H, F8>;
     constexpr int BN = Gm::BN, NS = Gm::NS, NWP = Gm::NWP, WSLOT = Gm::WSLOT, XST = Gm::XST;
+    constexpr int NP = Gm::NP, A_COL = Gm::A_COL, EW = Gm::EW, NJ = Gm::NJ, HALF_BYTES = Gm::HALF_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xs = smem + Gm::X_OFF;
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     const uint32_t tmem = *taddr_slot;
 
     if (warp < DQ0) {
-        regs_dec<REGS_WG0>();
+        regs_set<Regs<BH, H>::WG0>();
         if (warp == 0) {
             // ---------------- weight producer: units (k, k + 1) of a segment in
             // one 1-D bulk copy (a row block's units are consecutive)
@@ -610,7 +629,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         }
     } else if (warp < EPI0) {
         // ---------------- dequant: thread = weight row of the tile
-        regs_dec<Regs<H>::DQ>();
+        regs_set<Regs<BH, H>::DQ>();
         const int q = warp & 3;                           // tensor-memory lane quarter
         bool ok = true;
         int gi = 0, jp = 0;
@@ -619,13 +638,13 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const int k1 = (int)min((long long)G, k0 + (hi - u));
             const int codec = wide_tile(args, tile).P->codec;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NWP, WSLOT, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                ok = dequant_segment<8, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
                                                         tmem, q, lane, args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NWP, WSLOT, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                ok = dequant_segment<5, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
                                                         tmem, q, lane, args.status);
             else
-                ok = dequant_segment<4, NS, NWP, WSLOT, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
+                ok = dequant_segment<4, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
                                                         tmem, q, lane, args.status);
             u += k1 - k0;
         }
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     } else {
         // ---------------- epilogue: thread = row r of the tile, tokens
         // [64 c, 64 c + 64) of each 128-token half
-        regs_inc<Regs<H>::EPI>();
+        regs_set<Regs<BH, H>::EPI>();
         pdl_wait_prior();                                 // Y, R and the workspace follow the previous kernel
         const int q = warp & 3, c = (warp - EPI0) >> 2, e = warp - EPI0;
         const int r = q * 32 + lane;
@@ -643,11 +662,11 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         for (long long u = lo; u < hi && ok;) {
             const int tile = (int)(u / G), k0 = (int)(u % G);
             const int k1 = (int)min((long long)G, k0 + (hi - u));
-            float2 acc[H][32];
+            float2 acc[H][NJ];
 #pragma unroll
             for (int h = 0; h < H; ++h)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[h][j] = make_float2(0.f, 0.f);
+                for (int j = 0; j < NJ; ++j) acc[h][j] = make_float2(0.f, 0.f);
             for (int k = k0; k < k1 && ok; ++k, ++gi) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -662,8 +681,21 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                     // of this step could start)
                     const float sc = sc_ring[(gi % SC_RING) * BM + r];
                     const float2 s2 = make_float2(sc, sc);
-                    const uint32_t base = tmem + tl + P_COL + b * BH + 64 * c;
-                    if constexpr (H == 1) {
+                    const uint32_t base = tmem + tl + P_COL + b * BH + EW * c;
+                    if constexpr (EW == 32) {
+                        // one 32-column load per step
+                        uint32_t v[32];
+                        tc_ld32(base, v);
+                        tc_wait_ld();
+                        tc_regs_ready(v);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&pfree[b]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                              acc[h][i]);
+                    } else if constexpr (H == 1) {
                         // both loads in flight before one wait: the buffer is
                         // released one load latency after it filled
                         uint32_t v0[32], v1[32];
@@ -713,9 +745,9 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             // (the MMAs of the next segment run meanwhile)
             const WideTile tr = wide_tile(args, tile);
             const int n = tr.blk * BM + r;
-            const int t0 = tr.tt * BN + 64 * c;
+            const int t0 = tr.tt * BN + EW * c;
             if (k0 == 0 && k1 == G) {
-                store_tile<H, FUSED>(*tr.P, n, t0, T, acc);
+                store_tile<BH, H, NJ, FUSED>(*tr.P, n, t0, T, acc);
             } else {
                 const long long u0 = (long long)tile * G;
                 const int c_first = range_cta(U, gridDim.x, u0), c_last = range_cta(U, gridDim.x, u0 + G - 1);
@@ -724,8 +756,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < H; ++h)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int t = h * BH + 64 * c + 2 * j;
+                    for (int j = 0; j < NJ; ++j) {
+                        const int t = h * BH + EW * c + 2 * j;
                         mine[(size_t)t * BM + r] = acc[h][j].x;
                         mine[(size_t)(t + 1) * BM + r] = acc[h][j].y;
                     }
@@ -738,9 +770,9 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 if (old == (unsigned int)(c_last - c_first)) {
                     // the last of the tile's segments sums them all
                     __threadfence();
-                    fixup_sum<H, BN>(acc, args.part, U, (int)gridDim.x, c_first, c_last, u0, c, r);
+                    fixup_sum<BH, H, NJ, BN>(acc, args.part, U, (int)gridDim.x, c_first, c_last, u0, c, r);
                     if (lane == 0) *cnt = 0;              // zero again for the next run
-                    store_tile<H, FUSED>(*tr.P, n, t0, T, acc);
+                    store_tile<BH, H, NJ, FUSED>(*tr.P, n, t0, T, acc);
                 }
             }
             u += k1 - k0;
@@ -805,68 +837,67 @@ static cudaError_t make_xmap(CUtensorMap *map, const void *X, int T, int K, int 
 // than it saves.
 constexpr int MIN_UNITS_PER_CTA = 8;
 
-int wide_tile_tokens(int halves) { return halves * wide::BH; }
-
 // Workspace of the wide route for a plan of `rows` packed rows and widths up
 // to T_max: the partial-sum slots of one launch (two per CTA, sized for the
-// widest tile the plan can take) and the plan's split-tile counters (eight
-// per tile at the plan's largest tile count).
+// widest tile the plan can take: 256 tokens above T_max = 128, else 128) and
+// the plan's split-tile counters (eight per tile at the largest tile count any
+// of the route's widths gives, that of 64-token tiles).
+size_t wide_partial_bytes(int T_max, int sms) {
+    const int bn = T_max > 128 ? 256 : 128;
+    return (size_t)sms * 2 * bn * wide::BM * sizeof(float);
+}
+
 size_t wide_workspace_bytes(int rows, int T_max, int sms) {
     if (T_max <= 32) return 0;
     const int NB = (rows + wide::BM - 1) / wide::BM;
-    const int halves = T_max > wide::BH ? 2 : 1;
-    const size_t part = (size_t)sms * 2 * halves * wide::BH * wide::BM * sizeof(float);
-    const size_t tiles = (size_t)NB * ((T_max + wide::BH - 1) / wide::BH);   // at least the tiles of either width
-    return part + tiles * wide::EPI_WARPS * sizeof(unsigned int);
+    const size_t tiles = (size_t)NB * ((T_max + 63) / 64);
+    return wide_partial_bytes(T_max, sms) + tiles * wide::EPI_WARPS * sizeof(unsigned int);
 }
 
-size_t wide_partial_bytes(int T_max, int sms) {
-    const int halves = T_max > wide::BH ? 2 : 1;
-    return (size_t)sms * 2 * halves * wide::BH * wide::BM * sizeof(float);
-}
-
-template <int H, bool FUSED, bool F8>
+template <int BH, int H, bool FUSED, bool F8>
 static cudaError_t launch_t(const WideArgs &a, const CUtensorMap &xmap, int grid, bool pdl, cudaStream_t stream) {
     static std::atomic<bool> attr_set[64];
+    using Gm = wide::Geo<BH, H, F8>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(wide_kernel<H, FUSED, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 wide::Geo<H, F8>::BYTES);
+        e = cudaFuncSetAttribute(wide_kernel<BH, H, FUSED, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(wide::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = wide::Geo<H, F8>::BYTES;
+    cfg.dynamicSmemBytes = Gm::BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, wide_kernel<H, FUSED, F8>, a, xmap);
+    e = cudaLaunchKernelEx(&cfg, wide_kernel<BH, H, FUSED, F8>, a, xmap);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int H>
+template <int BH, int H>
 static cudaError_t launch_h(const WideArgs &a, const CUtensorMap &xmap, int grid, bool fused, bool f8, bool pdl,
                             cudaStream_t stream) {
-    if (f8) return fused ? launch_t<H, true, true>(a, xmap, grid, pdl, stream)
-                         : launch_t<H, false, true>(a, xmap, grid, pdl, stream);
-    return fused ? launch_t<H, true, false>(a, xmap, grid, pdl, stream)
-                 : launch_t<H, false, false>(a, xmap, grid, pdl, stream);
+    if (f8) return fused ? launch_t<BH, H, true, true>(a, xmap, grid, pdl, stream)
+                         : launch_t<BH, H, false, true>(a, xmap, grid, pdl, stream);
+    return fused ? launch_t<BH, H, true, false>(a, xmap, grid, pdl, stream)
+                 : launch_t<BH, H, false, false>(a, xmap, grid, pdl, stream);
 }
 
-// All parents (any mix of codecs) over one shared X in one launch of 128-token
-// (halves = 1) or 256-token (halves = 2) tiles.  part: the partial-sum slots
-// (wide_partial_bytes for this width); each parent's cnt its zeroed counters.
-cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int halves, float *part,
-                        unsigned int *status, bool pdl, int sms, cudaStream_t stream) {
-    const int BN = halves * wide::BH;
+// All parents (any mix of codecs) over one shared X in one launch of tiles of
+// BN = bh * halves tokens: bh = 64 (halves 1), or bh = 128 (halves 1 or 2).
+// part: the partial-sum slots (wide_partial_bytes covers the launch's width);
+// each parent's cnt its zeroed counters.  At most `sms` CTAs.
+cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int bh, int halves,
+                        float *part, unsigned int *status, bool pdl, int sms, cudaStream_t stream) {
+    if (!((bh == 64 && halves == 1) || (bh == 128 && (halves == 1 || halves == 2)))) return cudaErrorInvalidValue;
+    const int BN = halves * bh;
     CUtensorMap xmap;
     cudaError_t e = make_xmap(&xmap, X, T, K, BN);
     if (e != cudaSuccess) return e;
@@ -897,8 +928,9 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
     long long grid = a.units / MIN_UNITS_PER_CTA;
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    return halves == 2 ? launch_h<2>(a, xmap, (int)grid, fused, f8, pdl, stream)
-                       : launch_h<1>(a, xmap, (int)grid, fused, f8, pdl, stream);
+    if (bh == 64) return launch_h<64, 1>(a, xmap, (int)grid, fused, f8, pdl, stream);
+    return halves == 2 ? launch_h<128, 2>(a, xmap, (int)grid, fused, f8, pdl, stream)
+                       : launch_h<128, 1>(a, xmap, (int)grid, fused, f8, pdl, stream);
 }
 
 }  // namespace qg

@@ -1,7 +1,7 @@
 """GPU parity of the fused outputs against the fp64 oracle.
 
 Residual add (LinearAdd), the SwiGLU of a gate/up pair and bf16 output, on
-every route (8-, 16- and 32-token tiles, tensor-core tiles), both codecs,
+every route (8-, 16- and 32-token small-T tiles, the tcgen05 tiles), both codecs,
 ragged shapes, in place, with the argument errors of the extended entry
 points.  Tolerances are in tests/tolerance.py: the residual add keeps the
 GEMM's bound with |R| in the magnitude sum; SwiGLU propagates the gate and up
@@ -48,7 +48,8 @@ def _status_clean():
     assert qg.qgemm_device_status(clear=True) == qg.QGEMM_OK
 
 
-WIDTHS = [1, 5, 8, 13, 16, 30, 77, 300]          # every route: 8/16/32-token tiles and tcgen05
+WIDTHS = [1, 5, 8, 13, 16, 30, 77, 300]          # 8/16-token small-T tiles and the tcgen05 tiles
+SKINNY32 = 2                                       # the 32-token small-T route, forced below
 
 
 @pytest.mark.parametrize("T", WIDTHS)
@@ -158,3 +159,25 @@ def test_argument_errors():
     qg.check(qg.qgemm_run_ex(plain.plan, X, T, None, Y), "run_ex plain")
     torch.cuda.synchronize()
     assert torch.equal(y1, Y)
+
+
+@pytest.mark.parametrize("T", [17, 30])
+def test_fused_outputs_on_the_32_token_small_t_tile(T):
+    # the route table sends T = 17..32 to the tcgen05 route; the 32-token
+    # small-T tile, forced, still serves the fused outputs
+    N, K = 1000, 1024
+    p = synth.weights(25, N, K, 5)
+    x = synth.activations(25, T, K, outliers=True)
+    W = weights(p, T_max=64, epilogue=qg.QGEMM_EPILOGUE_ADD)
+    qg.check(qg.qgemm_plan_force_route(W.plan, SKINNY32), "force_route")
+    assert W.route(T) == "skinny32"
+    R = residual(25 + T, T, N)
+    Y = W.run(dev_x(x), R=torch.from_numpy(R).cuda())
+    Yref, A = oracle.linear_add(5, p["packed"], p["scales"], x, R, N, K)
+    assert_close(host(Y), Yref, A, f"add skinny32 T={T}")
+    gate, up = synth.weights(26, 203, K, 4, parent=0), synth.weights(26, 203, K, 4, parent=1)
+    P = pair(gate, up, T_max=64, out=qg.QGEMM_OUT_BF16)
+    qg.check(qg.qgemm_plan_force_route(P.plan, SKINNY32), "force_route")
+    Ys = P.run(dev_x(x))
+    out, g, u, Ag, Au = oracle.swiglu_pair(gate, up, x)
+    assert_close_swiglu(host(Ys), out, g, u, Ag, Au, f"swiglu bf16 skinny32 T={T}", bf16=True)

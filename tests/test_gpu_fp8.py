@@ -2,7 +2,8 @@
 
 Checked on every route: the small-T token tiles of 8, 16 and 32 (the
 straight-line kernel where K/64 is a multiple of 8, the ring kernel
-otherwise) and the tcgen05 tiles.  Every finite code decodes exactly (one-hot
+otherwise; the 32-token tile forced, since the route table sends T = 17..32
+to the tcgen05 route) and the tcgen05 tiles.  Every finite code decodes exactly (one-hot
 activations return s * value bitwise, subnormal codes included, on both
 kinds of route), parity at every width, ragged N, multi-parent launches
 mixing FP8 with int4, and the fused outputs on FP8 weights.
@@ -18,6 +19,8 @@ torch = pytest.importorskip("torch")
 qg = pytest.importorskip("bit_weight_only_groupwise_gb300")
 
 pytestmark = pytest.mark.gpu
+
+SKINNY32 = 2            # the 32-token small-T route, for qgemm_plan_force_route
 
 
 def dev_x(x_bits):
@@ -43,13 +46,15 @@ def _status_clean():
 def test_every_code_decodes_exactly(tw):
     # row n holds the finite codes in a rotated order; X = one-hot columns, so
     # Y[t][n] = s[n][k/64] * value(code[n][k]) with k = column t: exact in fp32.
-    # tw = 32 runs the 32-token small-T tile, 128 the tcgen05 tile.
+    # tw = 32 runs the 32-token small-T tile (forced), 128 the tcgen05 tile.
     N, K = 128, 512
     finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)        # 254 codes
     codes = np.stack([np.resize(np.roll(finite, 3 * n), K) for n in range(N)]).astype(np.uint8)
     scales = synth.group_scales(61, 1, N, K)
     p = {"bits": 8, "N": N, "K": K, "packed": codes, "scales": scales}
     W = weights(p, T_max=tw)
+    if tw == 32:
+        qg.check(qg.qgemm_plan_force_route(W.plan, SKINNY32), "force_route")
     ref_w = oracle.dequant(8, codes, scales, N, K)
     for k0 in range(0, K, tw):
         ks = np.arange(k0, k0 + tw)
@@ -61,10 +66,16 @@ def test_every_code_decodes_exactly(tw):
 
 @pytest.mark.parametrize("T", [1, 3, 8, 13, 16, 24, 32, 33, 100, 300])
 @pytest.mark.parametrize("N,K", [(5120, 6144), (1000, 1024), (130, 576), (300, 9216)])
-def test_parity(T, N, K):
-    # K = 576 (9 groups) and 9216 (144 groups) take the ring kernel at T <= 32
+@pytest.mark.parametrize("small_t_32", [False, True])
+def test_parity(T, N, K, small_t_32):
+    # K = 576 (9 groups) and 9216 (144 groups) take the ring kernel on the
+    # small-T tiles; small_t_32 forces the 32-token small-T tile for T <= 32
+    if small_t_32 and T > 32:
+        pytest.skip("the 32-token tile covers T <= 32")
     p = synth.weights(62, N, K, 8)
     W = weights(p, T_max=512)
+    if small_t_32:
+        qg.check(qg.qgemm_plan_force_route(W.plan, SKINNY32), "force_route")
     x = synth.activations(62, T, K, outliers=True)
     Y = W.run(dev_x(x))
     Yref, A = oracle.gemm_parent(p, x)

@@ -169,7 +169,7 @@ def test_domain_and_argument_errors():
     assert qg.qgemm_run_multi([W.plan, other.plan], X, 1, [Y, Y]) == qg.QGEMM_ERR_SHAPE
 
 
-@pytest.mark.parametrize("T", [1, 8, 16, 32, 40, 300])
+@pytest.mark.parametrize("T", [1, 8, 16, 32, 40, 300, 512])
 def test_one_route_per_call(T):
     p = synth.weights(2, 256, 512, 4)
     W = make_weights(p, T_max=512)
@@ -179,8 +179,9 @@ def test_one_route_per_call(T):
     W.run(X)
     launched = qg.qgemm_launch_count() - n0
     assert launched == 1, (route, launched)
-    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "skinny32" if T <= 32
-                     else "tcgen05_128x128" if T <= 128 else "tcgen05_128x256")
+    # 256 rows, 2 row blocks: the 128-token tile up to T = 511
+    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "tcgen05_128x64" if T <= 64
+                     else "tcgen05_128x128" if T < 512 else "tcgen05_128x256")
     n0 = qg.qgemm_launch_count()
     qg.GroupwiseWeights(4, 256, 512, p["packed"], p["scales"], T_max=8)
     assert qg.qgemm_launch_count() - n0 == 2            # pack + its ordering kernel

@@ -4,8 +4,8 @@ The route cuts the (tile, group) units of a launch into one contiguous range
 per CTA (stream-K), so a tile's 64-column groups may be summed by several
 CTAs: the last one to finish adds the others' partial sums from the plan's
 workspace in a fixed order.  These cases force many splits per tile, mix
-codecs over one activation in one launch, and run both tile widths (128 and
-256 tokens) on the same matrices; each result is compared element-wise with
+codecs over one activation in one launch, and run every tile width (64,
+128 and 256 tokens) on the same matrices; each result is compared element-wise with
 the fp64 oracle and repeated runs must be bit-identical (the split tiles'
 counters return to zero after every run).
 """
@@ -21,7 +21,7 @@ qg = pytest.importorskip("bit_weight_only_groupwise_gb300")
 
 pytestmark = pytest.mark.gpu
 
-WIDE128, WIDE256 = 3, 4
+SKINNY16, SKINNY32, WIDE128, WIDE256, WIDE64 = 1, 2, 3, 4, 5
 
 
 @pytest.fixture(autouse=True)
@@ -53,7 +53,7 @@ def check(p, x, Y, what, cols=None):
 
 
 @pytest.mark.parametrize("N,K,T", [(256, 8192, 40), (130, 4096, 200), (1000, 1024, 129), (128, 64, 33)])
-@pytest.mark.parametrize("route", [WIDE128, WIDE256])
+@pytest.mark.parametrize("route", [WIDE64, WIDE128, WIDE256])
 def test_split_tiles_match_the_oracle(N, K, T, route):
     # few tiles and many groups: each tile is split over many CTAs
     p = synth.weights(40, N, K, 4)
@@ -86,13 +86,13 @@ def test_mixed_codecs_share_one_launch(T):
 
 
 @pytest.mark.parametrize("bits", [4, 5, 8])
-def test_both_tile_widths_agree_with_the_oracle(bits):
+def test_every_tile_width_agrees_with_the_oracle(bits):
     N, K, T = 777, 3072, 520
     p = synth.weights(42, N, K, bits)
     x = synth.activations(42, T, K, outliers=True)
     X = dev_x(x)
     cols = wide_columns(T)
-    for route in (WIDE128, WIDE256):
+    for route in (WIDE64, WIDE128, WIDE256):
         W = weights(p, T_max=T, route=route)
         check(p, x, W.run(X), f"int{bits} {W.route(T)}", cols=cols)
 
@@ -101,8 +101,28 @@ def test_forcing_a_wide_route_needs_its_workspace():
     p = synth.weights(43, 256, 512, 4)
     small = weights(p, T_max=32)
     assert qg.qgemm_plan_force_route(small.plan, WIDE128) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_plan_force_route(small.plan, WIDE64) == qg.QGEMM_ERR_INVALID_ARG
     mid = weights(p, T_max=128)
     assert qg.qgemm_plan_force_route(mid.plan, WIDE256) == qg.QGEMM_ERR_INVALID_ARG
     assert qg.qgemm_plan_force_route(mid.plan, WIDE128) == qg.QGEMM_OK
+    assert qg.qgemm_plan_force_route(mid.plan, WIDE64) == qg.QGEMM_OK
     assert qg.qgemm_plan_force_route(mid.plan, -1) == qg.QGEMM_OK
     assert qg.qgemm_plan_force_route(mid.plan, 99) == qg.QGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("K", [6144, 576])
+@pytest.mark.parametrize("T", [9, 17, 24, 32])
+def test_forced_small_t_tiles(bits, K, T):
+    # the table sends T > 16 to the tcgen05 route; the 16- and 32-token
+    # small-T tiles (straight-line kernel at K = 6144, ring kernel at K = 576)
+    # still serve every T they cover when forced
+    p = synth.weights(44, 700, K, bits)
+    x = synth.activations(44, T, K, outliers=True)
+    X = dev_x(x)
+    for route in (SKINNY16, SKINNY32):
+        if route == SKINNY16 and T > 16:
+            continue
+        W = weights(p, T_max=64, route=route)
+        assert W.route(T) == ("skinny16" if route == SKINNY16 else "skinny32")
+        check(p, x, W.run(X), f"int{bits} K={K} T={T} {W.route(T)}")

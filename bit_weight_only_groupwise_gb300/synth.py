@@ -121,6 +121,36 @@ def fp64_to_fp16_bits(x: np.ndarray) -> np.ndarray:
 
 # ---------------------------------------------------------------- draws
 
+NVFP4 = 16   # codec id of NVFP4 weights (E2M1 codes, UE4M3 block scales, fp32 tensor scale)
+NVFP4_BLOCK = 16
+NVFP4_TENSOR_SCALE = 2.0 ** -8 * 1.25   # exact in fp32
+
+
+def nvfp4_codes(seed: int, tid: int, N: int, K: int) -> np.ndarray:
+    """uint8 E2M1 codes [N, K] (0..15), uniform over all sixteen patterns."""
+    z = draws(seed, tid, 0, N * K)
+    return (z >> np.uint64(60)).astype(np.uint8).reshape(N, K)
+
+
+def nvfp4_block_scales(seed: int, tid: int, N: int, K: int) -> np.ndarray:
+    """uint8 unsigned-E4M3 codes [N, ceil(K/16)]: exponent field uniform in 4..11,
+    mantissa uniform (values 2^-3 .. 30)."""
+    nb = (K + NVFP4_BLOCK - 1) // NVFP4_BLOCK
+    z = draws(seed, tid, 0, N * nb)
+    e = 4 + (z >> np.uint64(61)).astype(np.uint8)                  # 4 .. 11
+    m = ((z >> np.uint64(58)) & np.uint64(7)).astype(np.uint8)
+    return ((e << 3) | m).astype(np.uint8).reshape(N, nb)
+
+
+def pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """Raw 4-bit codes [N, K] two per byte: column 2j in bits 0-3, 2j+1 in bits 4-7."""
+    codes = np.asarray(codes, np.uint8)
+    N, K = codes.shape
+    if K % 2:
+        codes = np.concatenate([codes, np.zeros((N, 1), np.uint8)], axis=1)
+    return ((codes[:, 0::2] & 0x0F) | ((codes[:, 1::2] & 0x0F) << 4)).astype(np.uint8)
+
+
 def uniform_codes(seed: int, tid: int, N: int, K: int, bits: int) -> np.ndarray:
     """int8 codes [N, K], uniform over the b-bit two's-complement range; for
     bits = 8, uint8 E4M3 codes uniform over the 254 that are not NaN (a NaN
@@ -192,8 +222,13 @@ def pack_canonical(codes: np.ndarray, bits: int) -> np.ndarray:
 # ---------------------------------------------------------------- workloads
 
 def weights(seed: int, N: int, K: int, bits: int, parent: int = 0) -> dict:
-    """Codes, their canonical packing and group scales of one weight matrix."""
+    """Codes, their canonical packing and group scales of one weight matrix
+    (NVFP4, bits = 16: E2M1 codes, UE4M3 block scales and the tensor scale)."""
     off = 16 * parent
+    if bits == NVFP4:
+        codes = nvfp4_codes(seed, TID_CODES + off, N, K)
+        return {"bits": bits, "N": N, "K": K, "codes": codes, "packed": pack_nibbles(codes),
+                "scales": nvfp4_block_scales(seed, TID_SCALES + off, N, K), "tscale": NVFP4_TENSOR_SCALE}
     codes = uniform_codes(seed, TID_CODES + off, N, K, bits)
     return {
         "bits": bits,

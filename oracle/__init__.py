@@ -52,6 +52,12 @@ def _bind(lib):
     lib.qgemm_oracle_linear_add.restype = i32
     lib.qgemm_oracle_swiglu.argtypes = [i32, ptr, ptr, ptr]
     lib.qgemm_oracle_swiglu.restype = i32
+    lib.qgemm_oracle_nvfp4_blocks.argtypes = [i32]
+    lib.qgemm_oracle_nvfp4_blocks.restype = i32
+    lib.qgemm_oracle_dequant_nvfp4.argtypes = [i32, i32, ptr, ptr, ctypes.c_float, ptr]
+    lib.qgemm_oracle_dequant_nvfp4.restype = i32
+    lib.qgemm_oracle_gemm_nvfp4.argtypes = [i32, i32, i32, ptr, ptr, ctypes.c_float, ptr, ptr, ptr]
+    lib.qgemm_oracle_gemm_nvfp4.restype = i32
     return lib
 
 
@@ -114,8 +120,43 @@ def gemm(bits: int, packed: np.ndarray, scales: np.ndarray, x_bf16: np.ndarray,
     return Y, A
 
 
+NVFP4 = 16   # codec id of NVFP4 weights (E2M1 codes, UE4M3 scale per 16 columns, fp32 tensor scale)
+
+
+def dequant_nvfp4(codes_packed: np.ndarray, bscales: np.ndarray, tscale: float, N: int, K: int,
+                  lib=None) -> np.ndarray:
+    """fp64 W[n, k] = e2m1(c[n, k]) * ue4m3(b[n, k/16]) * tscale."""
+    lib = lib or load()
+    codes_packed = np.ascontiguousarray(codes_packed, dtype=np.uint8)
+    bscales = np.ascontiguousarray(bscales, dtype=np.uint8)
+    out = np.zeros((N, K), np.float64)
+    if lib.qgemm_oracle_dequant_nvfp4(N, K, _p(codes_packed), _p(bscales), float(tscale), _p(out)) != 0:
+        raise ValueError("oracle dequant_nvfp4: bad arguments")
+    return out
+
+
+def gemm_nvfp4(codes_packed: np.ndarray, bscales: np.ndarray, tscale: float, x_bf16: np.ndarray, N: int, K: int,
+               lib=None):
+    """(Y, A) of an NVFP4 matrix, as gemm() for the other codecs."""
+    lib = lib or load()
+    codes_packed = np.ascontiguousarray(codes_packed, dtype=np.uint8)
+    bscales = np.ascontiguousarray(bscales, dtype=np.uint8)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    T = x.shape[0]
+    assert x.shape == (T, K), (x.shape, T, K)
+    Y = np.zeros((T, N), np.float64)
+    A = np.zeros((T, N), np.float64)
+    if lib.qgemm_oracle_gemm_nvfp4(N, K, T, _p(codes_packed), _p(bscales), float(tscale), _p(x), _p(Y),
+                                   _p(A)) != 0:
+        raise ValueError("oracle gemm_nvfp4: bad arguments")
+    return Y, A
+
+
 def gemm_parent(parent: dict, x_bf16: np.ndarray, lib=None):
     """Oracle on one weight matrix as drawn by the input generator."""
+    if parent["bits"] == NVFP4:
+        return gemm_nvfp4(parent["packed"], parent["scales"], parent["tscale"], x_bf16, parent["N"], parent["K"],
+                          lib=lib)
     return gemm(parent["bits"], parent["packed"], parent["scales"], x_bf16,
                 parent["N"], parent["K"], lib=lib)
 

@@ -50,6 +50,20 @@
  *     SwiGLU:      out[t][f] = silu(g[t][f]) * u[t][f],  silu(z) = z / (1 + e^-z)
  *
  * with g and u the plain results of the gate and the up matrix.
+ *
+ * The NVFP4 codec (the "nvfp4" weight profile of the pages' RTX 5090
+ * publication index) is read here as the common NVFP4 definition: FP4 E2M1
+ * codes (sign, 2 exponent bits with bias 1, 1 mantissa bit, a subnormal at
+ * exponent 0: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one unsigned E4M3
+ * scale (4 exponent bits, bias 7, 3 mantissa bits, subnormals, no sign; the
+ * code 0x7F and codes with bit 7 set are outside the codec) per 16
+ * consecutive K-columns per row, and one fp32 scale for the whole tensor:
+ *
+ *     w[n][k] = e2m1(c[n][k]) * ue4m3(b[n][k/16]) * s_t
+ *
+ * Codes are packed two per byte like int4 (byte j: column 2j in bits 0-3,
+ * 2j+1 in bits 4-7); block scales are bytes [N][ceil(K/16)].  Every product
+ * x * w is exact in fp64 (8 + 2 + 4 + 24 significant bits).
  */
 #include <math.h>
 #include <stddef.h>
@@ -237,5 +251,91 @@ int qgemm_oracle_swiglu(int n, const double *g, const double *u, double *out)
         return -1;
     for (int i = 0; i < n; ++i)
         out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    return 0;
+}
+
+/* ------------------------------------------------------------------ NVFP4 */
+
+#define ORACLE_NVFP4_BLOCK 16
+
+/* FP4 E2M1 -> double, from the field definitions. */
+static double oracle_e2m1_to_double(int nib)
+{
+    int sign = (nib >> 3) & 1;
+    int expo = (nib >> 1) & 3;
+    int mant = nib & 1;
+    double v = expo == 0 ? 0.5 * mant                        /* subnormal: m/2 */
+                         : ldexp(1.0 + 0.5 * mant, expo - 1); /* (1 + m/2) * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+/* Unsigned E4M3 -> double; NaN for the codes outside the codec. */
+static double oracle_ue4m3_to_double(uint8_t b)
+{
+    int expo = (b >> 3) & 0x0f;
+    int mant = b & 0x07;
+    if ((b & 0x80) || (expo == 15 && mant == 7))
+        return NAN;
+    if (expo == 0)
+        return ldexp((double)mant, -9);                      /* subnormal: m/8 * 2^-6 */
+    return ldexp((double)(8 + mant), expo - 10);             /* (1 + m/8) * 2^(e-7) */
+}
+
+int qgemm_oracle_nvfp4_blocks(int K)
+{
+    return (K + ORACLE_NVFP4_BLOCK - 1) / ORACLE_NVFP4_BLOCK;
+}
+
+/* w[n][k] of an NVFP4 matrix into the scratch row w (K values). */
+static void oracle_nvfp4_row(int K, const uint8_t *codes_row, const uint8_t *bs_row, double ts, double *w)
+{
+    for (int k = 0; k < K; ++k) {
+        int byte = codes_row[k >> 1];
+        int nib = (k & 1) ? (byte >> 4) : (byte & 0x0f);
+        w[k] = oracle_e2m1_to_double(nib) * oracle_ue4m3_to_double(bs_row[k / ORACLE_NVFP4_BLOCK]) * ts;
+    }
+}
+
+/* Dequantised NVFP4 weights W[n][k], fp64 [N][K]. */
+int qgemm_oracle_dequant_nvfp4(int N, int K, const uint8_t *codes, const uint8_t *bscales, float tscale,
+                               double *W)
+{
+    if (N < 0 || K < 0)
+        return -1;
+    int rb = (K + 1) / 2, nb = qgemm_oracle_nvfp4_blocks(K);
+    for (int n = 0; n < N; ++n)
+        oracle_nvfp4_row(K, codes + (size_t)n * rb, bscales + (size_t)n * nb, (double)tscale, W + (size_t)n * K);
+    return 0;
+}
+
+/* Y[t][n] = sum_k x[t][k] * w[n][k] (k ascending) and A[t][n] = sum |x w|
+ * for an NVFP4 matrix, as qgemm_oracle_gemm does for the other codecs. */
+int qgemm_oracle_gemm_nvfp4(int N, int K, int T, const uint8_t *codes, const uint8_t *bscales, float tscale,
+                            const uint16_t *X, double *Y, double *A)
+{
+    if (N < 0 || K < 0 || T < 0)
+        return -1;
+    if (N == 0 || T == 0)
+        return 0;
+    int rb = (K + 1) / 2, nb = qgemm_oracle_nvfp4_blocks(K);
+    double *w = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    if (!w)
+        return -1;
+    for (int n = 0; n < N; ++n) {
+        oracle_nvfp4_row(K, codes + (size_t)n * rb, bscales + (size_t)n * nb, (double)tscale, w);
+        for (int t = 0; t < T; ++t) {
+            const uint16_t *xr = X + (size_t)t * K;
+            double acc = 0.0, mag = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double p = oracle_bf16_to_double(xr[k]) * w[k];
+                acc += p;
+                mag += fabs(p);
+            }
+            Y[(size_t)t * N + n] = acc;
+            if (A)
+                A[(size_t)t * N + n] = mag;
+        }
+    }
+    free(w);
     return 0;
 }

@@ -304,10 +304,64 @@ def pin_fp8_gemm(lib):
     assert np.allclose(A, mag, rtol=4 * K * U)
 
 
+# ------------------------------------------------------------ NVFP4
+
+# E2M1 magnitudes by the code's low three bits (exponent e, mantissa m): the
+# format's value set {0, 1/2, 1, 3/2, 2, 3, 4, 6}, written here as twice the
+# value, an integer, rather than from the exponent and mantissa fields
+E2M1_TWICE = [0, 1, 2, 3, 4, 6, 8, 12]
+
+
+def e2m1_values_table(codes):
+    codes = np.asarray(codes, np.int64)
+    mag = np.array(E2M1_TWICE, np.float64)[codes & 7] / 2.0
+    return np.where(codes & 8, -mag, mag)
+
+
+def ue4m3_values_torch(codes):
+    # an unsigned E4M3 code is an OCP E4M3 code with the sign bit clear
+    return fp8_values_torch(np.asarray(codes, np.uint8) & 0x7F)
+
+
+def pin_nvfp4_decode(lib):
+    # every E2M1 code against the value set, with a unit block and tensor scale
+    codes = np.arange(16, dtype=np.uint8).reshape(1, 16)
+    W = oracle.dequant_nvfp4(synth.pack_nibbles(codes), np.full((1, 1), 0x38, np.uint8), 1.0, 1, 16, lib=lib)[0]
+    assert np.array_equal(W, e2m1_values_table(codes[0]))
+    assert np.signbit(W[8]) and W[8] == 0.0                                 # code 8 is -0.0
+    # every unsigned E4M3 block scale (the E2M1 code 2 is 1.0) against torch
+    bs = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    ones = np.full((256, 16), 2, np.uint8)
+    Wb = oracle.dequant_nvfp4(synth.pack_nibbles(ones), bs, 1.0, 256, 16, lib=lib)[:, 0]
+    ref = ue4m3_values_torch(bs[:, 0])
+    outside = (bs[:, 0] >= 0x80) | (bs[:, 0] == 0x7F)
+    assert np.all(np.isnan(Wb[outside])) and not np.any(np.isnan(Wb[~outside]))
+    assert np.array_equal(Wb[~outside], ref[~outside])
+    assert (Wb[0x38], Wb[0x7E], Wb[0x01], Wb[0x08]) == (1.0, 448.0, 2.0 ** -9, 2.0 ** -6)
+
+
+def pin_nvfp4_gemm(lib):
+    # the whole formula against numpy on weights the test dequantises itself:
+    # one block scale per 16 columns, the tensor scale, nibble order
+    N, K, T = 13, 160, 4
+    p = synth.weights(52, N, K, synth.NVFP4)
+    x = synth.activations(52, T, K, outliers=True)
+    Y, A = oracle.gemm_parent(p, x, lib=lib)
+    w = e2m1_values_table(p["codes"]) * np.repeat(ue4m3_values_torch(p["scales"]), 16, axis=1)[:, :K] * p["tscale"]
+    xv = bf16_values(x)
+    ref = xv @ w.T
+    mag = np.abs(xv) @ np.abs(w).T
+    assert np.all(np.abs(Y - ref) <= 2 * K * U * mag)
+    assert np.allclose(A, mag, rtol=4 * K * U)
+    # a power-of-two tensor scale scales the result exactly
+    Y2, _ = oracle.gemm_nvfp4(p["packed"], p["scales"], 2 * p["tscale"], x, N, K, lib=lib)
+    assert np.array_equal(Y2, 2 * Y)
+
+
 PINS = [pin_golden, pin_exact_rational, pin_bruteforce_int4, pin_bruteforce_int5, pin_numpy_matmul,
         pin_linearity_exact, pin_identity_and_permutation, pin_scaling_and_negation,
         pin_int5_contains_int4, pin_column_independence, pin_swiglu, pin_linear_add, pin_fp8_decode,
-        pin_fp8_gemm]
+        pin_fp8_gemm, pin_nvfp4_decode, pin_nvfp4_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -341,6 +395,15 @@ MUTANTS = {
     "e4m3_subnormal": ("ldexp((double)mant, -9);", "ldexp((double)mant, -10);"),
     "e4m3_nan": ("if (expo == 15 && mant == 7)", "if (expo == 15)"),
     "e4m3_sign": ("int sign = b >> 7;", "int sign = (b >> 6) & 1;"),
+    "e2m1_bias": ("ldexp(1.0 + 0.5 * mant, expo - 1);", "ldexp(1.0 + 0.5 * mant, expo);"),
+    "e2m1_subnormal": ("expo == 0 ? 0.5 * mant", "expo == 0 ? 1.0 * mant"),
+    "e2m1_sign": ("int sign = (nib >> 3) & 1;", "int sign = (nib >> 2) & 1;"),
+    "nvfp4_block_width": ("#define ORACLE_NVFP4_BLOCK 16", "#define ORACLE_NVFP4_BLOCK 32"),
+    "nvfp4_tensor_scale_dropped": ("* oracle_ue4m3_to_double(bs_row[k / ORACLE_NVFP4_BLOCK]) * ts;",
+                                   "* oracle_ue4m3_to_double(bs_row[k / ORACLE_NVFP4_BLOCK]);"),
+    "ue4m3_signed": ("if ((b & 0x80) || (expo == 15 && mant == 7))", "if (expo == 15 && mant == 7)"),
+    "nvfp4_nibble_order": ("int nib = (k & 1) ? (byte >> 4) : (byte & 0x0f);\n        w[k]",
+                           "int nib = (k & 1) ? (byte & 0x0f) : (byte >> 4);\n        w[k]"),
 }
 
 

@@ -33,6 +33,7 @@ QGEMM_ERR_UNSUPPORTED = 8
 QGEMM_INT4 = 4
 QGEMM_INT5 = 5
 QGEMM_FP8 = 8
+QGEMM_NVFP4 = 16
 
 QGEMM_EPILOGUE_STORE = 0
 QGEMM_EPILOGUE_ADD = 1
@@ -47,7 +48,7 @@ EXPORTS = [
     "qgemm_plan_destroy", "qgemm_plan_route", "qgemm_route_name", "qgemm_launch_count",
     "qgemm_device_status", "qgemm_plan_set_pdl", "qgemm_pair_packed_bytes", "qgemm_pack_pair",
     "qgemm_plan_set_epilogue", "qgemm_run_ex", "qgemm_selftest_timeout", "qgemm_plan_force_route",
-    "qgemm_run_noalloc",
+    "qgemm_run_noalloc", "qgemm_plan_set_tensor_scale",
 ]
 
 _lock = threading.Lock()
@@ -85,6 +86,7 @@ def _declare(lib):
         "qgemm_selftest_timeout": ([vp], i32),
         "qgemm_plan_force_route": ([vp, i32], i32),
         "qgemm_run_noalloc": ([vp, vp, vp, i32, vp, vp], i32),
+        "qgemm_plan_set_tensor_scale": ([vp, c.c_float], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -196,6 +198,10 @@ def qgemm_run_ex(plan, X, T: int, R, Y, stream=None) -> int:
     return load().qgemm_run_ex(plan, _ptr(X), T, _ptr(R), _ptr(Y), _stream(stream))
 
 
+def qgemm_plan_set_tensor_scale(plan, scale: float) -> int:
+    return load().qgemm_plan_set_tensor_scale(plan, float(scale))
+
+
 def qgemm_plan_set_pdl(plan, enable: bool) -> int:
     return load().qgemm_plan_set_pdl(plan, 1 if enable else 0)
 
@@ -282,7 +288,8 @@ class GroupwiseWeights:
     """
 
     def __init__(self, codec: int, N: int, K: int, codes_canonical, scales_fp16, T_max: int,
-                 device="cuda", stream=None, epilogue: int = QGEMM_EPILOGUE_STORE, out: int = QGEMM_OUT_F32):
+                 device="cuda", stream=None, epilogue: int = QGEMM_EPILOGUE_STORE, out: int = QGEMM_OUT_F32,
+                 tensor_scale: float | None = None):
         import numpy as np
         import torch
         self.codec, self.N, self.K, self.T_max = codec, N, K, T_max
@@ -291,8 +298,10 @@ class GroupwiseWeights:
         if dev.type == "cuda" and dev.index is None:
             dev = torch.device("cuda", torch.cuda.current_device())
         self.device = dev
+        self.tensor_scale = tensor_scale
         codes = _to_dev(codes_canonical, np.uint8, dev)
-        scales = _to_dev(scales_fp16, np.int16, dev)
+        # NVFP4: UE4M3 block-scale bytes [N, K/16]; otherwise fp16 patterns
+        scales = _to_dev(scales_fp16, np.uint8 if codec == QGEMM_NVFP4 else np.int16, dev)
         nbytes = qgemm_packed_bytes(N, K, codec)
         if nbytes == 0:
             raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_packed_bytes")
@@ -306,6 +315,8 @@ class GroupwiseWeights:
         check(st, "qgemm_plan")
         if (self.epilogue, self.out) != (QGEMM_EPILOGUE_STORE, QGEMM_OUT_F32):
             check(qgemm_plan_set_epilogue(self.plan, self.epilogue, self.out), "qgemm_plan_set_epilogue")
+        if getattr(self, "tensor_scale", None) is not None:
+            check(qgemm_plan_set_tensor_scale(self.plan, self.tensor_scale), "qgemm_plan_set_tensor_scale")
         wsb = qgemm_plan_workspace_bytes(self.plan)
         self.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
         check(qgemm_plan_bind(self.plan, self.packed, self.workspace, self.workspace.numel()), "qgemm_plan_bind")
@@ -378,7 +389,7 @@ class SwiGLUPair(GroupwiseWeights):
     pair; ``run(X)`` returns silu(X . G^T) * (X . U^T), [T, F]."""
 
     def __init__(self, codec: int, F: int, K: int, gate_codes, gate_scales, up_codes, up_scales, T_max: int,
-                 device="cuda", stream=None, out: int = QGEMM_OUT_F32):
+                 device="cuda", stream=None, out: int = QGEMM_OUT_F32, tensor_scale: float | None = None):
         import numpy as np
         import torch
         self.codec, self.N, self.K, self.T_max = codec, F, K, T_max
@@ -391,7 +402,9 @@ class SwiGLUPair(GroupwiseWeights):
         if nbytes == 0:
             raise QgemmError(QGEMM_ERR_SHAPE, "qgemm_pair_packed_bytes")
         self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        check(qgemm_pack_pair(codec, F, K, _to_dev(gate_codes, np.uint8, dev), _to_dev(gate_scales, np.int16, dev),
-                              _to_dev(up_codes, np.uint8, dev), _to_dev(up_scales, np.int16, dev), self.packed,
+        self.tensor_scale = tensor_scale
+        sdt = np.uint8 if codec == QGEMM_NVFP4 else np.int16
+        check(qgemm_pack_pair(codec, F, K, _to_dev(gate_codes, np.uint8, dev), _to_dev(gate_scales, sdt, dev),
+                              _to_dev(up_codes, np.uint8, dev), _to_dev(up_scales, sdt, dev), self.packed,
                               stream), "qgemm_pack_pair")
         self._make_plan(dev)

@@ -84,6 +84,7 @@ struct qgemm_plan_s {
     int sms;
     bool pdl;              // launch with programmatic dependent launch
     int forced_route;      // -1: the route table; else qgemm_plan_force_route's route
+    float tscale;          // NVFP4: the tensor scale (qgemm_plan_set_tensor_scale)
     size_t ws_bytes;       // workspace the plan's routes need (the tcgen05 routes' split tiles)
     size_t ws_part;        // of it, the partial-sum slots (the counters follow)
     const uint8_t *packed;
@@ -123,7 +124,7 @@ static unsigned int *status_ptr() {
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5 || c == QGEMM_FP8; }
+static bool valid_codec(int c) { return c == QGEMM_INT4 || c == QGEMM_INT5 || c == QGEMM_FP8 || c == QGEMM_NVFP4; }
 
 extern "C" {
 
@@ -191,6 +192,7 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
     p->sms = sms;
     p->pdl = true;
     p->forced_route = -1;
+    p->tscale = 1.0f;
     p->ws_bytes = wide_workspace_bytes(N, T_max, sms);
     p->ws_part = p->ws_bytes ? wide_partial_bytes(T_max, sms) : 0;
     *out = p;
@@ -250,6 +252,12 @@ qgemm_status qgemm_plan_set_epilogue(qgemm_plan_t plan, qgemm_epilogue epilogue,
     plan->NB = (plan->rows + BLOCK_ROWS - 1) / BLOCK_ROWS;
     plan->ws_bytes = wide_workspace_bytes(plan->rows, plan->T_max, plan->sms);
     plan->ws_part = plan->ws_bytes ? wide_partial_bytes(plan->T_max, plan->sms) : 0;
+    return QGEMM_OK;
+}
+
+qgemm_status qgemm_plan_set_tensor_scale(qgemm_plan_t plan, float scale) {
+    if (!plan || plan->codec != QGEMM_NVFP4) return QGEMM_ERR_INVALID_ARG;
+    plan->tscale = scale;
     return QGEMM_OK;
 }
 
@@ -319,6 +327,7 @@ static void fill_parent(SkinnyParent &sp, const qgemm_plan_s *p, void *Y, const 
     sp.R = R;
     sp.N = p->rows;
     sp.codec = p->codec;
+    sp.tscale = p->tscale;
     sp.cta_begin = cta_begin;
     sp.ncols = p->N;
     sp.epi = p->epi;
@@ -351,6 +360,7 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
             wp[i].cnt = reinterpret_cast<unsigned int *>(plans[i]->ws + plans[i]->ws_part);
             wp[i].N = plans[i]->rows;
             wp[i].codec = plans[i]->codec;
+            wp[i].tscale = plans[i]->tscale;
             wp[i].ncols = plans[i]->N;
             wp[i].epi = plans[i]->epi;
             wp[i].ybf16 = plans[i]->out == QGEMM_OUT_BF16;
@@ -376,7 +386,7 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
     a.K = K;
     a.G = G;
     bool f8 = false;
-    for (int i = 0; i < np; ++i) f8 = f8 || plans[i]->codec == QGEMM_FP8;
+    for (int i = 0; i < np; ++i) f8 = f8 || plans[i]->codec == QGEMM_FP8 || plans[i]->codec == QGEMM_NVFP4;
     // the straight-line kernel (8 groups per warp, all in flight) where K / 64
     // is a multiple of 8, else the ring kernel with 8 warps per CTA
     const int nj = skinny_line_groups(G, 8);
@@ -512,6 +522,7 @@ extern "C" qgemm_status qgemm_run_noalloc(qgemm_plan_t plan, const void *packed_
     wp.cnt = reinterpret_cast<unsigned int *>(scratch);
     wp.N = plan->rows;
     wp.codec = plan->codec;
+    wp.tscale = plan->tscale;
     wp.ncols = plan->N;
     wp.epi = plan->epi;
     if (launch_wide(&wp, 1, X, T, plan->K, 128, halves, reinterpret_cast<float *>(scratch + NOALLOC_COUNTER_BYTES),

@@ -62,9 +62,12 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
         const uint8_t *src = sr.which ? canon_up : canon;
         const int k0 = grp * GROUP + 16 * c;
         for (int j = 0; j < 16; ++j) {
-            int ub;                                   // biased code
+            int ub;                                   // biased code (NVFP4: the raw E2M1 code)
             if (row < 0) {
-                ub = codec == 5 ? 16 : 8;
+                ub = codec == 5 ? 16 : codec == NVFP4 ? 0 : 8;
+            } else if (codec == NVFP4) {
+                const uint8_t byte = src[(size_t)row * (K / 2) + (k0 + j) / 2];
+                ub = ((k0 + j) & 1) ? (byte >> 4) : (byte & 15);
             } else if (codec == 4) {
                 const uint8_t byte = src[(size_t)row * (K / 2) + (k0 + j) / 2];
                 const int nib = ((k0 + j) & 1) ? (byte >> 4) : (byte & 15);
@@ -87,7 +90,17 @@ __global__ void __launch_bounds__(256) pack_kernel(int codec, int N, int K, cons
     *reinterpret_cast<uint4 *>(u + w * 512 + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
     if (codec == 5) *reinterpret_cast<uint32_t *>(u + NIB_BYTES + w * 128 + lane * 4) = hi;
     }
-    if (c == 0) {
+    if (codec == NVFP4) {
+        // the lane's block (c) of rows r0 and r1: UE4M3 bytes [rows][K/16]
+        const uint8_t *bs = reinterpret_cast<const uint8_t *>(scales);
+        const uint8_t *bs_up = reinterpret_cast<const uint8_t *>(scales_up);
+        const int KB = K / 16;
+        const SrcRow a0 = src_row(b * BLOCK_ROWS + 16 * w + g, N, F);
+        const SrcRow a1 = src_row(b * BLOCK_ROWS + 16 * w + g + 8, N, F);
+        const uint32_t b0 = a0.row >= 0 ? (a0.which ? bs_up : bs)[(size_t)a0.row * KB + grp * 4 + c] : 0;
+        const uint32_t b1 = a1.row >= 0 ? (a1.which ? bs_up : bs)[(size_t)a1.row * KB + grp * 4 + c] : 0;
+        *reinterpret_cast<uint16_t *>(u + NIB_BYTES + w * 64 + lane * 2) = (uint16_t)(b0 | (b1 << 8));
+    } else if (c == 0) {
         const SrcRow a0 = src_row(b * BLOCK_ROWS + 16 * w + g, N, F);
         const SrcRow a1 = src_row(b * BLOCK_ROWS + 16 * w + g + 8, N, F);
         const uint16_t s0 = a0.row >= 0 ? (a0.which ? scales_up : scales)[(size_t)a0.row * G + grp] : 0;

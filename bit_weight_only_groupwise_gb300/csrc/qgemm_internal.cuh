@@ -30,6 +30,13 @@
 // code plane (8 tiles x 1024 B) is followed by the scales as above.  Padding
 // rows hold code 0 (+0.0) and s = 0.
 //
+// NVFP4 units: the nibble plane as for int4, holding the raw E2M1 codes (no
+// bias; padding rows hold code 0, +0.0), then the UE4M3 block scales: 8 tiles
+// x 32 lanes x 2 B, lane l = 4g + c of tile w holding the scale bytes of rows
+// r0 and r1 for the lane's 16 columns (block c of the group).  The fp32
+// tensor scale travels with the launch and takes the place of the per-group
+// rescale.
+//
 // Decode: OR a biased code into the mantissa of bf16 128.0 (0x4300; the
 // mantissa of [128, 256) counts in steps of 1) and subtract 128 + bias: the
 // result is the exact integer q as bf16, with no integer-to-float conversion.
@@ -54,10 +61,14 @@ constexpr int UNIT4 = NIB_BYTES + SCALE_BYTES;
 constexpr int UNIT5 = NIB_BYTES + HI_BYTES + SCALE_BYTES;
 constexpr int CODE8_BYTES = 8192;          // fp8 code plane of a unit: 8 tiles x 32 lanes x 32 B
 constexpr int UNIT8 = CODE8_BYTES + SCALE_BYTES;
+constexpr int NVFP4 = 16;                  // codec id of NVFP4 weights
+constexpr int BS_BYTES = 512;              // NVFP4 block scales of a unit: 8 tiles x 32 lanes x 2 B
+constexpr int UNIT16 = NIB_BYTES + BS_BYTES;
 
 __host__ __device__ constexpr int unit_bytes(int codec) {
-    return codec == 8 ? UNIT8 : codec == 5 ? UNIT5 : UNIT4;
+    return codec == NVFP4 ? UNIT16 : codec == 8 ? UNIT8 : codec == 5 ? UNIT5 : UNIT4;
 }
+// offset of the scales in a unit (the block scales for NVFP4)
 __host__ __device__ constexpr int scale_off(int codec) {
     return codec == 8 ? CODE8_BYTES : codec == 5 ? NIB_BYTES + HI_BYTES : NIB_BYTES;
 }
@@ -86,6 +97,7 @@ struct SkinnyParent {
     const uint8_t *packed;   // units of this parent
     void *Y;                 // [T][ncols], fp32 or bf16
     const float *R;          // EPI_ADD: residual [T][ncols]
+    float tscale;            // NVFP4: the tensor scale (in place of the group scales)
     int N, codec;            // N: packed rows
     int cta_begin;           // first CTA of this parent in the grid
     int ncols;               // columns of Y: N, or F of a SwiGLU pair (N = pair_rows(F))
@@ -108,6 +120,7 @@ struct WideParent {
     void *Y;                 // [T][ncols], fp32 or bf16
     const float *R;          // EPI_ADD: residual [T][ncols]
     unsigned int *cnt;       // this parent's split-tile counters (zero between runs)
+    float tscale;            // NVFP4: the tensor scale (in place of the group scales)
     int N, codec;            // N: packed rows
     int cta_begin;           // first output tile of this parent in its launch
     int nblocks;             // 128-row blocks
@@ -323,6 +336,28 @@ __device__ __forceinline__ uint32_t dec8_pair(uint32_t w) {
     const uint32_t mag = (SHI ? (w >> 4) : (w << 4)) & 0x07F007F0u;
     const uint32_t sgn = SHI ? w : (w << 8);
     return bf16x2_mul(and_or(sgn, 0x80008000u, mag), 0x7B807B80u);   // x 2^120
+}
+
+// NVFP4: two E2M1 codes (nibble positions I and I + 4 of w, the k pair
+// (2I, 2I + 1)) times the block scale pair bs2, as an exact bf16x2 pair.  A
+// code's exponent and mantissa bits placed at bf16 bits 6..8 read as the
+// code's value times 2^-126 (the subnormal code included: bf16's own
+// subnormal), its sign goes to bit 15; one bf16x2 multiply by 2^126 and one
+// by the block scale give the value (E2M1 has 2 significant bits, UE4M3 4: the
+// product is exact, between 2^-10 and 2688).
+template <int I>
+__device__ __forceinline__ uint32_t dec16_pair(uint32_t w, uint32_t bs2) {
+    constexpr int MS = 6 - 4 * I, SS = 12 - 4 * I;   // shifts of the magnitude and sign bits
+    const uint32_t mag = (MS >= 0 ? (w << MS) : (w >> (-MS))) & 0x01C001C0u;
+    const uint32_t sgn = w << SS;
+    return bf16x2_mul(bf16x2_mul(and_or(sgn, 0x80008000u, mag), 0x7E807E80u), bs2);   // x 2^126, x scale
+}
+
+// Two UE4M3 block-scale bytes (bits 0..7 and 8..15 of b) as a bf16x2 pair:
+// the code's 7 bits at bf16 bits 4..10 read as its value times 2^-120.
+__device__ __forceinline__ uint32_t ue4m3x2_to_bf16x2(uint32_t b) {
+    const uint32_t lo = b & 0xFFu, hi = (b >> 8) & 0xFFu;
+    return bf16x2_mul(((lo << 4) | (hi << 20)) & 0x07F007F0u, 0x7B807B80u);   // x 2^120
 }
 
 // int5: nibble pair plus the two high bits taken from the lane's high word.

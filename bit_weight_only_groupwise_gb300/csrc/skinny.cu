@@ -117,6 +117,17 @@ __device__ __forceinline__ void decode_tile(int codec, uint4 cw, uint32_t hw, ui
     }
 }
 
+// NVFP4 A fragments: the lane's nibble words as for int4 (x, y row g; z, w row
+// g+8) times the rows' block scales (bytes 0 and 1 of bsw), exact in bf16.
+__device__ __forceinline__ void decode_tile16(uint4 cw, uint32_t bsw, uint32_t (&a)[4][4]) {
+    const uint32_t bsp = ue4m3x2_to_bf16x2(bsw);
+    const uint32_t b0 = __byte_perm(bsp, 0, 0x1010), b1 = __byte_perm(bsp, 0, 0x3232);
+    a[0][0] = dec16_pair<0>(cw.x, b0); a[0][1] = dec16_pair<0>(cw.z, b1); a[0][2] = dec16_pair<1>(cw.x, b0); a[0][3] = dec16_pair<1>(cw.z, b1);
+    a[1][0] = dec16_pair<2>(cw.x, b0); a[1][1] = dec16_pair<2>(cw.z, b1); a[1][2] = dec16_pair<3>(cw.x, b0); a[1][3] = dec16_pair<3>(cw.z, b1);
+    a[2][0] = dec16_pair<0>(cw.y, b0); a[2][1] = dec16_pair<0>(cw.w, b1); a[2][2] = dec16_pair<1>(cw.y, b0); a[2][3] = dec16_pair<1>(cw.w, b1);
+    a[3][0] = dec16_pair<2>(cw.y, b0); a[3][1] = dec16_pair<2>(cw.w, b1); a[3][2] = dec16_pair<3>(cw.y, b0); a[3][3] = dec16_pair<3>(cw.w, b1);
+}
+
 // FP8 A fragments from the lane's 32-byte chunk: lo = row g, hi = row g+8,
 // word q of a row = k 4q .. 4q+3 (pairs in bytes 0/2 and 1/3).
 __device__ __forceinline__ void decode_tile8(uint4 lo, uint4 hi, uint32_t (&a)[4][4]) {
@@ -164,16 +175,19 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
     const int nj = (G - kw + KW - 1) / KW;           // groups of this warp: kw + KW*j
 
     // per-lane copy plan: every lane its 16-byte code chunk (FP8: 32 bytes,
-    // two copies); lanes 8..15 the int5 high words; lanes 16..17 the scale pairs
+    // two copies); lanes 8..15 the int5 high words, or lanes 8..11 the NVFP4
+    // block scales; lanes 16..17 the scale pairs (not NVFP4: its tensor scale
+    // stands in for them)
     const bool f8 = ST == STAGE8 && codec == 8;
+    const bool fp4 = ST == STAGE8 && codec == NVFP4;
     const int ch = f8 ? 32 : 16;                     // code bytes per lane
     const int sco = f8 ? SC8 : 640;                  // scale pairs in the stage
     const uint8_t *src = P.packed + ((size_t)b * G + kw) * UB + w * 32 * ch + lane * ch;
     const size_t step = (size_t)KW * UB;
-    const bool cp_hi = codec == 5 && lane >= 8 && lane < 16;
-    const bool cp_sc = lane >= 16 && lane < 18;
+    const bool cp_hi = (codec == 5 && lane >= 8 && lane < 16) || (fp4 && lane >= 8 && lane < 12);
+    const bool cp_sc = !fp4 && lane >= 16 && lane < 18;
     const int ex_dst = cp_hi ? 512 + (lane - 8) * 16 : sco + (lane - 16) * 16;
-    const long ex_src = cp_hi ? (long)(NIB_BYTES + w * 128 + (lane - 8) * 16) - (w * 512 + lane * 16)
+    const long ex_src = cp_hi ? (long)(NIB_BYTES + w * (fp4 ? 64 : 128) + (lane - 8) * 16) - (w * 512 + lane * 16)
                               : (long)(scale_off(codec) + w * 32 + (lane - 16) * 16) - (w * 32 * ch + lane * ch);
     const bool cp_ex = cp_hi || cp_sc;
 
@@ -239,8 +253,10 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
                 uint8_t *st = ring + r * ST;
                 const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * ch);
                 const uint4 cw8 = f8 ? *reinterpret_cast<const uint4 *>(st + lane * ch + 16) : make_uint4(0, 0, 0, 0);
-                const uint32_t hw = codec == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
-                const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + sco + g * 4);
+                const uint32_t hw = codec == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4)
+                                    : fp4      ? *reinterpret_cast<const uint16_t *>(st + 512 + lane * 2)
+                                               : 0u;
+                const uint32_t sp = fp4 ? 0u : *reinterpret_cast<const uint32_t *>(st + sco + g * 4);
                 __syncwarp();                         // every lane has read the stage
                 if (j0 + r + RING < nj) {
                     cp_async16(st + lane * ch, src_next);
@@ -258,8 +274,10 @@ __global__ void __launch_bounds__(KW * 32) skinny_kernel(const __grid_constant__
 
                 uint32_t a[4][4];
                 if (f8) decode_tile8(cw, cw8, a);
+                else if (fp4) decode_tile16(cw, hw, a);
                 else decode_tile(codec, cw, hw, a);
-                const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
+                const float2 sc = fp4 ? make_float2(P.tscale, P.tscale)
+                                      : __half22float2(*reinterpret_cast<const __half2 *>(&sp));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -368,7 +386,7 @@ __device__ __forceinline__ void issue_groups(std::integer_sequence<int, R...>, u
 template <int NT, int CODEC, int NJ, int RG, int XP, int R>
 __device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, int lane, int g,
                                            const __nv_bfloat16 *const (&xr)[NT], const uint32_t (&xpre)[XP][8],
-                                           float (&acc)[NT][4]) {
+                                           float (&acc)[NT][4], float ts) {
     constexpr int UB = unit_bytes(CODEC);
     using S = LineStage<UB>;
     constexpr int ISSUED = RG + R < NJ ? RG + R : NJ;     // groups whose copies are issued
@@ -385,16 +403,19 @@ __device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, 
     const uint8_t *st = ring + (R % RG) * S::BYTES;
     const uint4 cw = *reinterpret_cast<const uint4 *>(st + lane * S::CH);
     const uint4 cw8 = S::F8 ? *reinterpret_cast<const uint4 *>(st + lane * S::CH + 16) : make_uint4(0, 0, 0, 0);
-    const uint32_t hw = CODEC == 5 ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4) : 0u;
-    const uint32_t sp = *reinterpret_cast<const uint32_t *>(st + S::SC + g * 4);
+    const uint32_t hw = CODEC == 5       ? *reinterpret_cast<const uint32_t *>(st + 512 + lane * 4)
+                        : CODEC == NVFP4 ? *reinterpret_cast<const uint16_t *>(st + 512 + lane * 2)
+                                         : 0u;
+    const uint32_t sp = CODEC == NVFP4 ? 0u : *reinterpret_cast<const uint32_t *>(st + S::SC + g * 4);
     if (R + RG < NJ) {
         __syncwarp();                                  // every lane has read the stage
         issue_group<UB, RG, R + RG>(ring, lc, lane);
     }
     uint32_t a[4][4];
     if (S::F8) decode_tile8(cw, cw8, a);
+    else if (CODEC == NVFP4) decode_tile16(cw, hw, a);
     else decode_tile(CODEC, cw, hw, a);
-    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(&sp));
+    const float2 sc = CODEC == NVFP4 ? make_float2(ts, ts) : __half22float2(*reinterpret_cast<const __half2 *>(&sp));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         float p[4] = {0.f, 0.f, 0.f, 0.f};
@@ -413,8 +434,8 @@ __device__ __forceinline__ void line_group(uint8_t *ring, const LaneCopies &lc, 
 template <int NT, int CODEC, int NJ, int RG, int XP, int... R>
 __device__ __forceinline__ void line_groups(std::integer_sequence<int, R...>, uint8_t *ring, const LaneCopies &lc,
                                             int lane, int g, const __nv_bfloat16 *const (&xr)[NT],
-                                            const uint32_t (&xpre)[XP][8], float (&acc)[NT][4]) {
-    (line_group<NT, CODEC, NJ, RG, XP, R>(ring, lc, lane, g, xr, xpre, acc), ...);
+                                            const uint32_t (&xpre)[XP][8], float (&acc)[NT][4], float ts) {
+    (line_group<NT, CODEC, NJ, RG, XP, R>(ring, lc, lane, g, xr, xpre, acc, ts), ...);
 }
 
 template <int XP, int... R>
@@ -441,15 +462,15 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
     float *red = reinterpret_cast<float *>(smem + LineSmem<NJ, RG, NT>::rings(KW, S::BYTES));
 
     // per-lane copy plan (as the ring kernel's): every lane its 16-byte code
-    // chunk (FP8: 32 bytes); lanes 8..15 the int5 high words; lanes 16..17 the
-    // scale pairs
-    const bool cp_hi = CODEC == 5 && lane >= 8 && lane < 16;
+    // chunk (FP8: 32 bytes); lanes 8..15 the int5 high words, or 8..11 the
+    // NVFP4 block scales; lanes 16..17 the scale pairs (not for NVFP4)
+    const bool cp_hi = (CODEC == 5 && lane >= 8 && lane < 16) || (CODEC == NVFP4 && lane >= 8 && lane < 12);
     const int own = w * 32 * S::CH + lane * S::CH;    // the lane's chunk in the unit
     LaneCopies lc;
     lc.src = P.packed + ((size_t)b * G + gb) * UB + own;
-    lc.ex = cp_hi || (lane >= 16 && lane < 18);
+    lc.ex = cp_hi || (CODEC != NVFP4 && lane >= 16 && lane < 18);
     lc.ex_dst = cp_hi ? 512 + (lane - 8) * 16 : S::SC + (lane - 16) * 16;
-    lc.ex_src = cp_hi ? (NIB_BYTES + w * 128 + (lane - 8) * 16) - own
+    lc.ex_src = cp_hi ? (NIB_BYTES + w * (CODEC == NVFP4 ? 64 : 128) + (lane - 8) * 16) - own
                       : (scale_off(CODEC) + w * 32 + (lane - 16) * 16) - own;
     issue_groups<UB, RG>(std::make_integer_sequence<int, RG>{}, ring, lc, lane);
     // Programmatic dependent launch: with one token tile the next kernel in the
@@ -486,7 +507,8 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    line_groups<NT, CODEC, NJ, RG, XP>(std::make_integer_sequence<int, NJ>{}, ring, lc, lane, g, xr, xpre, acc);
+    line_groups<NT, CODEC, NJ, RG, XP>(std::make_integer_sequence<int, NJ>{}, ring, lc, lane, g, xr, xpre, acc,
+                                       P.tscale);
     if (NT > 1 && threadIdx.x == 0) pdl_launch_dependents();
 
     // ---- combine the warps' partials in warp order and write Y
@@ -503,9 +525,9 @@ __device__ __forceinline__ void line_tile(const SkinnyArgs &args, const SkinnyPa
     write_tile<RS>(P, red, T8, KW, tile, T);
 }
 
-// F8: the launch has FP8 parents (the kernel then also serves the integer
-// codecs, for multi-parent launches); the integer-only instantiation keeps
-// the code of the integer codecs alone.
+// F8: the launch has FP8 or NVFP4 parents (the kernel then also serves the
+// integer codecs, for multi-parent launches); the integer-only instantiation
+// keeps the code of the integer codecs alone.
 template <int NT, int NJ, int RG, bool F8>
 __global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_constant__ SkinnyArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -516,6 +538,7 @@ __global__ void __launch_bounds__(16 * 32) skinny_line_kernel(const __grid_const
     const SkinnyParent &P = args.p[pi];
     const int tile = blockIdx.x - P.cta_begin;
     if (F8 && P.codec == 8) line_tile<NT, 8, NJ, RG>(args, P, tile, smem);
+    else if (F8 && P.codec == NVFP4) line_tile<NT, NVFP4, NJ, RG>(args, P, tile, smem);
     else if (P.codec == 4) line_tile<NT, 4, NJ, RG>(args, P, tile, smem);
     else line_tile<NT, 5, NJ, RG>(args, P, tile, smem);
 }
@@ -550,24 +573,16 @@ static cudaError_t launch_line_t(const SkinnyArgs &a, int grid, bool pdl, cudaSt
 }
 
 // Groups per warp of the straight-line kernel that serves K / 64 = G groups
-// (at most 16 warps per CTA): 0 if none does.  nj_pref 16 selects 16 groups
-// per warp through an 8-stage ring where G allows, 8 selects 8 groups per
-// warp all in flight.
+// (at most 16 warps per CTA): 8, all in flight, or 0 if none does.  (16
+// groups per warp through an 8-stage ring measured slower and is gone.)
 int skinny_line_groups(int G, int nj_pref) {
-    if (nj_pref == 16 && G % 16 == 0 && G / 16 <= 16) return 16;
     if (nj_pref >= 8 && G % 8 == 0 && G / 8 <= 16) return 8;
     return 0;
 }
 
 template <bool F8>
 static cudaError_t launch_line_f(const SkinnyArgs &a, int nt, int nj, int grid, bool pdl, cudaStream_t stream) {
-    if (nj == 16 && a.G % 16 == 0 && a.G / 16 <= 16) {
-        switch (nt) {
-            case 1: return launch_line_t<1, 16, 8, F8>(a, grid, pdl, stream);
-            case 2: return launch_line_t<2, 16, 8, F8>(a, grid, pdl, stream);
-            case 4: return launch_line_t<4, 16, 8, F8>(a, grid, pdl, stream);
-        }
-    } else if (nj == 8 && a.G % 8 == 0 && a.G / 8 <= 16) {
+    if (nj == 8 && a.G % 8 == 0 && a.G / 8 <= 16) {
         switch (nt) {
             case 1: return launch_line_t<1, 8, 8, F8>(a, grid, pdl, stream);
             case 2: return launch_line_t<2, 8, 8, F8>(a, grid, pdl, stream);
@@ -622,17 +637,11 @@ static cudaError_t launch_skinny_s(const SkinnyArgs &a, int nt, int kw, int grid
             case 2: return launch_skinny_t<2, 8, ST>(a, grid, pdl, stream);
             case 4: return launch_skinny_t<4, 8, ST>(a, grid, pdl, stream);
         }
-    } else if (kw == 4) {
-        switch (nt) {
-            case 1: return launch_skinny_t<1, 4, ST>(a, grid, pdl, stream);
-            case 2: return launch_skinny_t<2, 4, ST>(a, grid, pdl, stream);
-            case 4: return launch_skinny_t<4, 4, ST>(a, grid, pdl, stream);
-        }
     }
     return cudaErrorInvalidValue;
 }
 
-// Tokens per launch: 8 * nt with nt in {1, 2, 4}; kw warps per CTA in {4, 8};
+// Tokens per launch: 8 * nt with nt in {1, 2, 4}; kw = 8 warps per CTA;
 // f8: some parent holds FP8 codes (larger stages).
 cudaError_t launch_skinny(const SkinnyArgs &a, int nt, int kw, int grid, bool pdl, bool f8, cudaStream_t stream) {
     return f8 ? launch_skinny_s<STAGE8>(a, nt, kw, grid, pdl, stream)

@@ -266,11 +266,27 @@ template <int BH, int H> struct Regs {
 // ---------------------------------------------------------------- dequant
 
 // Weight row r of a unit in shared memory as 32 bf16x2 words in natural k
-// order (word m = columns 2m, 2m + 1), and its fp16 scale.
+// order (word m = columns 2m, 2m + 1), and the scale of its group: the fp16
+// scale, or for NVFP4 (codes times their block scales) the tensor scale ts.
 template <int CODEC>
-__device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&av)[32]) {
+__device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&av)[32], float ts) {
     const int tile = r >> 4, i = r & 15, gi_ = i & 7, half = i >> 3;
-    if constexpr (CODEC == 8) {
+    if constexpr (CODEC == NVFP4) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(u + tile * 512 + (4 * gi_ + c) * 16 + 8 * half);
+            const uint32_t bsb = u[NIB_BYTES + tile * 64 + (4 * gi_ + c) * 2 + half];   // block c of row r
+            const uint32_t bs2 = ue4m3x2_to_bf16x2(bsb | (bsb << 8));
+            const uint32_t wv[2] = {v.x, v.y};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t *o = av + 8 * c + 4 * h;
+                o[0] = dec16_pair<0>(wv[h], bs2); o[1] = dec16_pair<1>(wv[h], bs2);
+                o[2] = dec16_pair<2>(wv[h], bs2); o[3] = dec16_pair<3>(wv[h], bs2);
+            }
+        }
+        return ts;
+    } else if constexpr (CODEC == 8) {
         // E4M3: the row's 16 codes of lane chunk c (k 16c .. 16c+15)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -317,7 +333,7 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 template <int CODEC, int NS, int NWP, int WSLOT, int A_COL, bool PAIR>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
-                                                float *sc_ring, uint32_t tmem, int q, int lane,
+                                                float *sc_ring, uint32_t tmem, int q, int lane, float ts,
                                                 unsigned int *status) {
     using namespace wide;
     constexpr int UB = unit_bytes(CODEC);
@@ -329,8 +345,8 @@ __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp
         if (!mbar_wait_warp(&w_full[wsl], (jp / NWP) & 1, status)) return false;
         if constexpr (PAIR) {
             uint32_t av[2][32];
-            sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT, r, av[0]);
-            if (n == 2) sc_ring[((gi + 1) % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + UB, r, av[1]);
+            sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT, r, av[0], ts);
+            if (n == 2) sc_ring[((gi + 1) % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + UB, r, av[1], ts);
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[wsl]);
             // A stages of both units were last read by the MMAs of units gi - NA
@@ -360,7 +376,7 @@ __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp
         } else {
             for (int e = 0; e < n; ++e, ++gi) {
                 uint32_t av[32];
-                sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + e * UB, r, av);
+                sc_ring[(gi % SC_RING) * BM + r] = decode_row<CODEC>(ws + wsl * WSLOT + e * UB, r, av, ts);
                 if (e == n - 1) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&w_empty[wsl]);
@@ -494,7 +510,7 @@ __device__ __forceinline__ void fixup_sum(float2 (&acc)[H][NJ], const float *par
 // fused output (residual add, SwiGLU or bf16); the plain instantiation keeps
 // the store loop, and the code, of the plain GEMM (the fused store code in
 // every launch measured 12% slower at T = 4096).  F8: a parent holds FP8
-// codes.  Parents of different codecs share one launch: the codec is
+// or NVFP4 codes.  Parents of different codecs share one launch: the codec is
 // resolved per tile.
 template <int BH, int H, bool FUSED, bool F8>
 __global__ void __launch_bounds__(wide::THREADS, 1)
@@ -636,16 +652,22 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         for (long long u = lo; u < hi && ok;) {
             const int tile = (int)(u / G), k0 = (int)(u % G);
             const int k1 = (int)min((long long)G, k0 + (hi - u));
-            const int codec = wide_tile(args, tile).P->codec;
+            const WideParent &P = *wide_tile(args, tile).P;
+            const int codec = P.codec;
+            const float ts = P.tscale;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
-                                                        tmem, q, lane, args.status);
+                ok = dequant_segment<8, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                      xa_empty, sc_ring, tmem, q, lane, ts, args.status);
+            else if (F8 && codec == NVFP4)
+                ok = dequant_segment<NVFP4, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                          xa_empty, sc_ring, tmem, q, lane, ts,
+                                                                          args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
-                                                        tmem, q, lane, args.status);
+                ok = dequant_segment<5, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             else
-                ok = dequant_segment<4, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full, xa_empty, sc_ring,
-                                                        tmem, q, lane, args.status);
+                ok = dequant_segment<4, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             u += k1 - k0;
         }
         if (!ok && lane == 0) *abort_flag = 1;
@@ -913,7 +935,7 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
         d.nblocks = (parents[i].N + wide::BM - 1) / wide::BM;
         tiles += d.nblocks * ntt;
         fused = fused || parents[i].epi != EPI_STORE || parents[i].ybf16;
-        f8 = f8 || parents[i].codec == 8;
+        f8 = f8 || parents[i].codec == 8 || parents[i].codec == NVFP4;
     }
     a.T = T;
     a.K = K;

@@ -36,7 +36,20 @@
  *         same fp16 scale per 64 columns.  FP8 is the weight-only FP8 format
  *         of the FP8-weight kernel the "Speculative decoding" page checks at
  *         verify widths; every route serves it.
- *   scales: fp16 bit patterns, row-major [N][K/64].
+ *   nvfp4: K/2 bytes per row like int4 (column 2j in bits 0-3, 2j+1 in bits
+ *         4-7), each nibble an FP4 E2M1 code (sign, 2 exponent bits with bias
+ *         1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), weighted
+ *         by an unsigned E4M3 scale per 16 columns per row (bias 7, subnormals;
+ *         0x7F and codes with bit 7 set are outside the codec) and by one fp32
+ *         scale for the whole matrix (qgemm_plan_set_tensor_scale):
+ *         deq(W)[n][k] = e2m1(c[n][k]) * ue4m3(b[n][k/16]) * s_t.  This is the
+ *         "nvfp4" weight profile of "ninfer-3080 docs/performance.md" (RTX
+ *         5090 publication index), read as the common NVFP4 definition.
+ *         E2M1 times UE4M3 is exact in bf16, so the kernels multiply each code
+ *         by its block scale in the decode and apply s_t where the other codecs
+ *         apply their group scales.
+ *   scales: fp16 bit patterns, row-major [N][K/64]; for NVFP4 the same
+ *         argument points to the UE4M3 block-scale bytes, row-major [N][K/16].
  *
  * Conventions for every call
  *   - All pointers named *_dev and X, Y are device pointers (or managed /
@@ -75,7 +88,7 @@ typedef enum {
     QGEMM_ERR_UNSUPPORTED = 8      /* no usable GPU of the architecture this library was built for */
 } qgemm_status;
 
-typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5, QGEMM_FP8 = 8 } qgemm_codec;
+typedef enum { QGEMM_INT4 = 4, QGEMM_INT5 = 5, QGEMM_FP8 = 8, QGEMM_NVFP4 = 16 } qgemm_codec;
 
 typedef struct qgemm_plan_s *qgemm_plan_t;
 
@@ -262,6 +275,16 @@ qgemm_status qgemm_run_ex(qgemm_plan_t plan, const void *X, int T, const void *R
  * Errors: QGEMM_ERR_INVALID_ARG (NULL plan).
  */
 qgemm_status qgemm_plan_set_pdl(qgemm_plan_t plan, int enable);
+
+/*
+ * The fp32 tensor scale s_t of an NVFP4 plan (1.0 until set).  It applies to
+ * the runs that follow; set it before capturing runs into a CUDA graph.
+ * Passage: the "nvfp4" weight profile of "ninfer-3080 docs/performance.md"
+ * (RTX 5090 publication index); the per-tensor scale is part of the NVFP4
+ * format read there.
+ * Errors: QGEMM_ERR_INVALID_ARG (NULL plan, or a plan of another codec).
+ */
+qgemm_status qgemm_plan_set_tensor_scale(qgemm_plan_t plan, float scale);
 
 /*
  * Route the plan takes at width T (a small integer naming the kernel family

@@ -20,6 +20,7 @@ int main(void)
         (any_fn)qgemm_launch_count, (any_fn)qgemm_device_status, (any_fn)qgemm_selftest_timeout,
         (any_fn)qgemm_pair_packed_bytes, (any_fn)qgemm_pack_pair, (any_fn)qgemm_plan_set_epilogue,
         (any_fn)qgemm_run_ex, (any_fn)qgemm_plan_force_route, (any_fn)qgemm_run_noalloc,
+        (any_fn)qgemm_plan_set_tensor_scale,
     };
     for (size_t i = 0; i < sizeof fns / sizeof fns[0]; ++i)
         if (!fns[i])

@@ -65,6 +65,9 @@ WIDTHS = {
     "swiglu": [1, 2, 4, 8],
     "decode_fp8": [1, 2, 4, 8],
     "prefill_fp8": [256, 1024, 4096],
+    "decode_nvfp4": [1, 2, 4, 8],
+    "prefill_nvfp4": [256, 1024, 4096],
+    "decode_ring": [1, 8, 16],
 }
 # a workload is a list of configurations; one step is one call at every width of each
 WORKLOADS = {"all": ["tiny", "decode", "batched", "multi", "prefill_a", "prefill_b"]}
@@ -72,11 +75,11 @@ WORKLOADS.update({name: [name] for name in WIDTHS})
 
 
 def codec_name(bits: int) -> str:
-    return "fp8" if bits == 8 else f"int{bits}"
+    return {8: "fp8", synth.NVFP4: "nvfp4"}.get(bits, f"int{bits}")
 
 
 def codec_bits(codec: str) -> int:
-    return 8 if codec == "fp8" else int(codec[3:])
+    return {"fp8": 8, "nvfp4": synth.NVFP4}.get(codec) or int(codec[3:])
 
 
 def describe(name: str) -> dict:
@@ -90,7 +93,10 @@ def describe(name: str) -> dict:
 
 
 def weight_bytes(N: int, K: int, bits: int) -> int:
-    # algorithmic: packed codes + fp16 group scales, read once per call
+    # algorithmic: packed codes + their scales, read once per call (fp16 per
+    # 64 columns; NVFP4: 4-bit codes and one byte per 16 columns)
+    if bits == synth.NVFP4:
+        return N * K // 2 + N * (K // 16)
     return N * K * bits // 8 + 2 * N * (K // 64)
 
 
@@ -273,7 +279,10 @@ def _oracle_call(lib, wl, cfg, T, rows=None, r0=0):
             n = min(rows, N)
             idx = (r0 + np.arange(n)) % N
             t0 = time.perf_counter()
-            oracle.gemm(p["bits"], p["packed"][idx], p["scales"][idx], x, n, K, lib=lib)
+            if p["bits"] == synth.NVFP4:
+                oracle.gemm_nvfp4(p["packed"][idx], p["scales"][idx], p["tscale"], x, n, K, lib=lib)
+            else:
+                oracle.gemm(p["bits"], p["packed"][idx], p["scales"][idx], x, n, K, lib=lib)
             dt = time.perf_counter() - t0
         elapsed += dt * (T + 1) / (cols + 1)
         done += weight_bytes(n, K, p["bits"]) + 2 * T * K * n / N
@@ -357,7 +366,7 @@ def run_reference(args, desc):
 class Config:
     """One configuration's weights (R packed copies, one plan each), inputs and outputs."""
 
-    def __init__(self, qg, torch, dev, cfg, copies, pdl):
+    def __init__(self, qg, torch, dev, cfg, copies, pdl, force_route=-1):
         self.cfg = cfg
         K = cfg["K"]
         Ts = cfg["T"]
@@ -375,7 +384,8 @@ class Config:
             self.set_bytes = qg.qgemm_pair_packed_bytes(g["N"], K, g["bits"])
             self.out_cols = [g["N"]]
         else:
-            base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max, epilogue=epi_code)
+            base = [qg.GroupwiseWeights(p["bits"], p["N"], K, p["packed"], p["scales"], T_max, epilogue=epi_code,
+                                        tensor_scale=p.get("tscale"))
                     for p in parents]
             self.set_bytes = sum(qg.qgemm_packed_bytes(p["N"], K, p["bits"]) for p in parents)
             self.out_cols = [p["N"] for p in parents]
@@ -395,6 +405,10 @@ class Config:
                 w.workspace = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
                 qg.check(qg.qgemm_plan_bind(w.plan, w.packed, w.workspace, w.workspace.numel()), "bind")
                 qg.check(qg.qgemm_plan_set_pdl(w.plan, pdl), "set_pdl")
+                if getattr(b, "tensor_scale", None) is not None:
+                    qg.check(qg.qgemm_plan_set_tensor_scale(w.plan, b.tensor_scale), "set_tensor_scale")
+                if force_route >= 0:
+                    qg.check(qg.qgemm_plan_force_route(w.plan, force_route), "force_route")
                 ws.append(w)
             self.sets.append(ws)
         self.xs = {T: torch.from_numpy(wl["x"][:T].view(np.int16).copy()).to(dev) for T in Ts}
@@ -446,7 +460,7 @@ def run_ours(args, desc):
     for c in desc["configs"]:
         set_bytes = sum(qg.qgemm_packed_bytes(p["N"], c["K"], codec_bits(p["codec"])) for p in c["parents"])
         copies = R if len(desc["configs"]) > 1 else max(R, min(256, int(np.ceil(3 * L2_BYTES / set_bytes))))
-        cfgs.append(Config(qg, torch, dev, c, copies, not args.no_pdl))
+        cfgs.append(Config(qg, torch, dev, c, copies, not args.no_pdl, args.force_route))
     torch.cuda.synchronize()
 
     # eager warm-up (loads the kernels), then one CUDA graph per (call, chunk
@@ -614,6 +628,8 @@ def run_ours(args, desc):
         config = config_summary(desc)
         config.update({"l2": l2, "parallelism": "replicas" if world > 1 else "single", "pdl": not args.no_pdl,
                        "calls_per_graph": R})
+        if args.force_route >= 0:
+            config["forced_route"] = args.force_route
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -643,6 +659,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="all")
     ap.add_argument("--calls-per-graph", type=int, default=10,
                     help="R: calls of one (configuration, width) per CUDA graph (a divisor of --steps)")
+    ap.add_argument("--force-route", type=int, default=-1,
+                    help="route sweeps and profiles: force this route (qgemm_plan_force_route) where it covers T")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")

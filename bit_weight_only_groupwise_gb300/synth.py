@@ -259,6 +259,11 @@ CONFIGS = {
     # the decode shape with FP8 (E4M3) weights at decode and verify widths
     "decode_fp8": dict(parents=[(5120, 8)], K=6144, Ts=[1, 2, 4, 8], outliers=True),
     "prefill_fp8": dict(parents=[(7168, 8)], K=5120, Ts=[256, 1024, 4096], outliers=True),
+    # NVFP4 weights at decode and prefill widths
+    "decode_nvfp4": dict(parents=[(5120, NVFP4)], K=6144, Ts=[1, 2, 4, 8], outliers=True),
+    "prefill_nvfp4": dict(parents=[(7168, NVFP4)], K=5120, Ts=[256, 1024, 4096], outliers=True),
+    # K / 64 = 90 groups, not a multiple of 8: the small-T route's ring kernel
+    "decode_ring": dict(parents=[(5120, 4)], K=5760, Ts=[1, 8, 16], outliers=True),
 }
 
 

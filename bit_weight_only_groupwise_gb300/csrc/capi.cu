@@ -24,6 +24,7 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
                         float *part, unsigned int *status, bool pdl, int sms, cudaStream_t stream);
 size_t wide_workspace_bytes(int rows, int T_max, int sms);
 size_t wide_partial_bytes(int T_max, int sms);
+int wide_max_tokens(int T_max);
 }  // namespace qg
 
 using namespace qg;
@@ -273,11 +274,11 @@ int qgemm_plan_route(qgemm_plan_t plan, int T) {
 }
 
 // Whether the plan's workspace holds what `route` needs: the tcgen05 routes
-// keep partial sums sized by T_max (128-token tiles above T_max = 32,
-// 256-token tiles above 128).
+// keep partial sums of their token tile, and a plan's workspace is sized for
+// the widest tile its T_max can take (64 tokens above T_max = 16, 128 above
+// 64, 256 above 128).
 static bool workspace_fits(const qgemm_plan_s *p, int route) {
-    if (!wide_route(route)) return true;
-    return p->T_max > 32 && (route != ROUTE_WIDE256 || p->T_max > 128);
+    return !wide_route(route) || route_tokens(route) <= wide_max_tokens(p->T_max);
 }
 
 qgemm_status qgemm_plan_force_route(qgemm_plan_t plan, int route) {

@@ -861,16 +861,17 @@ constexpr int MIN_UNITS_PER_CTA = 8;
 
 // Workspace of the wide route for a plan of `rows` packed rows and widths up
 // to T_max: the partial-sum slots of one launch (two per CTA, sized for the
-// widest tile the plan can take: 256 tokens above T_max = 128, else 128) and
-// the plan's split-tile counters (eight per tile at the largest tile count any
-// of the route's widths gives, that of 64-token tiles).
+// widest token tile the plan's widths can take, wide_max_tokens) and the
+// plan's split-tile counters (eight per tile at the largest tile count any of
+// the route's widths gives, that of 64-token tiles).
+int wide_max_tokens(int T_max) { return T_max <= 16 ? 0 : T_max <= 64 ? 64 : T_max <= 128 ? 128 : 256; }
+
 size_t wide_partial_bytes(int T_max, int sms) {
-    const int bn = T_max > 128 ? 256 : 128;
-    return (size_t)sms * 2 * bn * wide::BM * sizeof(float);
+    return (size_t)sms * 2 * wide_max_tokens(T_max) * wide::BM * sizeof(float);
 }
 
 size_t wide_workspace_bytes(int rows, int T_max, int sms) {
-    if (T_max <= 32) return 0;
+    if (wide_max_tokens(T_max) == 0) return 0;
     const int NB = (rows + wide::BM - 1) / wide::BM;
     const size_t tiles = (size_t)NB * ((T_max + 63) / 64);
     return wide_partial_bytes(T_max, sms) + tiles * wide::EPI_WARPS * sizeof(unsigned int);

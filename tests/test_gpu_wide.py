@@ -99,9 +99,13 @@ def test_every_tile_width_agrees_with_the_oracle(bits):
 
 def test_forcing_a_wide_route_needs_its_workspace():
     p = synth.weights(43, 256, 512, 4)
+    tiny = weights(p, T_max=16)
+    assert qg.qgemm_plan_workspace_bytes(tiny.plan) == 0
+    assert qg.qgemm_plan_force_route(tiny.plan, WIDE64) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_plan_force_route(tiny.plan, WIDE128) == qg.QGEMM_ERR_INVALID_ARG
     small = weights(p, T_max=32)
     assert qg.qgemm_plan_force_route(small.plan, WIDE128) == qg.QGEMM_ERR_INVALID_ARG
-    assert qg.qgemm_plan_force_route(small.plan, WIDE64) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_plan_force_route(small.plan, WIDE64) == qg.QGEMM_OK
     mid = weights(p, T_max=128)
     assert qg.qgemm_plan_force_route(mid.plan, WIDE256) == qg.QGEMM_ERR_INVALID_ARG
     assert qg.qgemm_plan_force_route(mid.plan, WIDE128) == qg.QGEMM_OK
@@ -126,3 +130,17 @@ def test_forced_small_t_tiles(bits, K, T):
         W = weights(p, T_max=64, route=route)
         assert W.route(T) == ("skinny16" if route == SKINNY16 else "skinny32")
         check(p, x, W.run(X), f"int{bits} K={K} T={T} {W.route(T)}")
+
+
+@pytest.mark.parametrize("T_max", [17, 32, 64])
+def test_table_route_within_a_narrow_domain(T_max):
+    # a plan whose widths stop between 17 and 64 has the workspace of the
+    # 64-token tcgen05 tile the table picks for T > 16
+    N, K = 1000, 1024
+    p = synth.weights(45, N, K, 4)
+    W = weights(p, T_max=T_max)
+    assert qg.qgemm_plan_workspace_bytes(W.plan) > 0
+    for T in sorted({17, T_max}):
+        x = synth.activations(45 + T, T, K, outliers=True)
+        assert W.route(T) == "tcgen05_128x64"
+        check(p, x, W.run(dev_x(x)), f"T_max={T_max} T={T} {W.route(T)}")

@@ -39,9 +39,9 @@
 //                 by the row's fp16 scale and accumulate in fp32 registers
 //                 (packed f32x2 FMA); write Y, or a partial sum and its count.
 // A step is one 128-token half of one group: step j = unit * H + h.
-// Tensor memory: NP = 3 P buffers of 128 columns (step j uses j mod 3, so
-// the epilogue has two steps of MMA time to drain a buffer) and NA = 4 A
-// stages of 32 columns.  Barriers:
+// Tensor memory: NA A stages of 32 columns (4; 8 for the 64-token tile) and
+// NP P buffers of 128 or 64 columns in the rest (step j uses j mod NP, so the
+// epilogue has NP - 1 steps of MMA time to drain a buffer).  Barriers:
 //   xa_full[s]   A_g stored (4 dequant warps) and X_g landed (TMA bytes)
 //   xa_empty[s]  the MMAs of both halves of group g completed (one commit
 //                per step): X stage s and A stage g mod NA are free
@@ -61,7 +61,6 @@ namespace qg {
 namespace wide {
 
 constexpr int BM = 128;                   // weight rows per tile (tensor-memory lanes)
-constexpr int NA = 4;                     // A stages in tensor memory (unit u uses u mod NA)
 constexpr int DQ_WARPS = 4;               // one dequant warp per tensor-memory lane quarter
 constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
 constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
@@ -69,16 +68,19 @@ constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
 constexpr int SC_RING = 16;               // units of scales in flight
 constexpr int P_COL = 0;                  // P buffers from column 0, then the A stages
 constexpr int TMEM_COLS = 512;
-constexpr int X_REGION = 128 * 1024;      // activation stages
 
 // BH: tokens per MMA (64 or 128); H: MMAs ("halves") per tile, so BN = BH H
-// tokens; F8: a parent of the launch holds FP8 codes (larger units, so fewer
-// weight stages fit).  Tensor memory holds the A stages and as many P buffers
-// of BH columns as fit beside them: 3 of 128 columns or 6 of 64, so that the
-// epilogue has NP - 1 steps of MMA time to drain a buffer.
+// tokens; F8: a parent of the launch holds FP8 or NVFP4 codes (larger units,
+// so fewer weight stages fit).  Tensor memory holds the A stages and as many
+// P buffers of BH columns as fit beside them: 3 of 128 columns beside 4 A
+// stages, or 4 of 64 beside 8.  The 64-token tile's dequant is the step that
+// limits it (a unit's MMAs are short), so it gets twice the A stages, half
+// the activation stages (its X tiles are half as large) and twice the weight
+// stages, and runs four unit pairs ahead of the MMAs instead of two.
 template <int BH_, int H, bool F8>
 struct Geo {
     static constexpr int BH = BH_;
+    static constexpr int NA = BH == 64 ? 8 : 4;           // A stages (unit u uses u mod NA)
     static constexpr int NP = (TMEM_COLS - 32 * NA) / BH;  // P buffers (step j uses j mod NP)
     static constexpr int A_COL = P_COL + NP * BH;         // A stages: 32 columns each
     static constexpr int EW = BH / 2;                     // P columns per epilogue warp
@@ -86,9 +88,10 @@ struct Geo {
     static constexpr int HALF_BYTES = BH * GROUP * 2;     // one MMA's X tile of one group
     static constexpr int BN = H * BH;
     static constexpr int XST = H * HALF_BYTES;           // X stage: BN tokens x 64 columns
-    static constexpr int NS = X_REGION / XST;             // 16, 8 or 4 stages
+    static constexpr int X_REGION = BH == 64 ? 64 * 1024 : 128 * 1024;  // activation stages
+    static constexpr int NS = X_REGION / XST;             // 8 (64- and 128-token tiles) or 4 stages
     static constexpr int WSLOT = 2 * (F8 ? UNIT8 : UNIT5);
-    static constexpr int NWP = F8 ? 4 : 6;                // weight stages (pairs of units)
+    static constexpr int NWP = BH == 64 ? (F8 ? 8 : 12) : (F8 ? 4 : 6);  // weight stages (pairs of units)
     static constexpr int X_OFF = 0;                       // 1024-aligned (128B swizzle atoms)
     static constexpr int W_OFF = X_REGION;
     static constexpr int BAR_OFF = W_OFF + NWP * WSLOT;
@@ -146,19 +149,25 @@ __device__ __forceinline__ int range_cta(long long U, int grid, long long u) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D(tmem) (+)= A(tmem) . B(smem desc)^T, bf16 inputs, fp32 accumulate
-__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool accum) {
+// D(tmem) (+)= A(tmem) . B(smem desc)^T, bf16 inputs, fp32 accumulate, issued
+// by one lane of a converged warp that the instruction itself elects (a
+// predicate, not a branch around the instruction).
+__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool accum) {
     asm volatile(
-        "{.reg .pred p; setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
+        "{.reg .pred e, p; elect.sync _|e, 0xffffffff; setp.ne.u32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
         ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(accum ? 1u : 0u) : "memory");
 }
 
-// arrive on an mbarrier once all previously issued MMAs of this thread complete
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
+// Commits of all previously issued MMAs of the elected lane to two mbarriers.
+__device__ __forceinline__ void tc_commit2_elect(uint64_t *bar0, uint64_t *bar1) {
+    asm volatile(
+        "{.reg .pred e; elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];}"
+        ::"r"(smem_u32(bar0)), "r"(smem_u32(bar1)) : "memory");
 }
+
 
 #define QG_R32(a) a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[8], a[9], a[10], a[11], a[12], a[13], a[14], \
                   a[15], a[16], a[17], a[18], a[19], a[20], a[21], a[22], a[23], a[24], a[25], a[26], a[27], a[28], \
@@ -257,9 +266,9 @@ __device__ __forceinline__ void regs_set() {
 // The 128-token tile's dequant decodes a pair of units at once (more
 // registers); the 256-token tile's epilogue holds twice the accumulators.
 template <int BH, int H> struct Regs {
-    static constexpr int WG0 = 40;
-    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 96;
-    static constexpr int EPI = BH == 64 ? 152 : H == 1 ? 160 : 184;
+    static constexpr int WG0 = H == 2 ? 24 : 40;
+    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 72;
+    static constexpr int EPI = BH == 64 ? 152 : H == 1 ? 160 : 208;
     static_assert(128 * (WG0 + DQ) + 256 * EPI <= 512 * REGS_AT_LAUNCH, "register split");
 };
 
@@ -330,7 +339,7 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 // two units (the integer codecs on the 128-token tile, where a unit's MMAs
 // are short); otherwise one unit at a time (fewer live registers: the FP8
 // decode, the 256-token tile's accumulators).
-template <int CODEC, int NS, int NWP, int WSLOT, int A_COL, bool PAIR>
+template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
                                                 float *sc_ring, uint32_t tmem, int q, int lane, float ts,
@@ -518,7 +527,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     using namespace wide;
     using Gm = Geo<BH, H, F8>;
     constexpr int BN = Gm::BN, NS = Gm::NS, NWP = Gm::NWP, WSLOT = Gm::WSLOT, XST = Gm::XST;
-    constexpr int NP = Gm::NP, A_COL = Gm::A_COL, EW = Gm::EW, NJ = Gm::NJ, HALF_BYTES = Gm::HALF_BYTES;
+    constexpr int NA = Gm::NA, NP = Gm::NP, A_COL = Gm::A_COL, EW = Gm::EW, NJ = Gm::NJ, HALF_BYTES = Gm::HALF_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xs = smem + Gm::X_OFF;
@@ -625,15 +634,11 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 const uint32_t d = tmem + P_COL + b * BH;
                 const uint32_t a = tmem + A_COL + (gi % NA) * 32;
                 const uint32_t b0 = smem_u32(xs + s * XST + h * HALF_BYTES);
-                // one elected lane per instruction: measured cheaper to issue
-                // than one elected block of four
+                // one lane elected by each instruction (predicated, no branch)
 #pragma unroll
                 for (int kk = 0; kk < GROUP / 16; ++kk)
-                    if (elect_one()) tc_mma_ts(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
-                if (elect_one()) {
-                    tc_commit(&pfull[b]);
-                    tc_commit(&xa_empty[s]);
-                }
+                    tc_mma_ts_elect(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
+                tc_commit2_elect(&pfull[b], &xa_empty[s]);
                 __syncwarp();
                 last = j;
             }
@@ -656,17 +661,17 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const int codec = P.codec;
             const float ts = P.tscale;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             else if (F8 && codec == NVFP4)
-                ok = dequant_segment<NVFP4, NS, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                           xa_empty, sc_ring, tmem, q, lane, ts,
                                                                           args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             else
-                ok = dequant_segment<4, NS, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             u += k1 - k0;
         }
@@ -717,7 +722,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                         for (int i = 0; i < 16; ++i)
                             acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
                                               acc[h][i]);
-                    } else if constexpr (H == 1) {
+                    } else {
                         // both loads in flight before one wait: the buffer is
                         // released one load latency after it filled
                         uint32_t v0[32], v1[32];
@@ -736,28 +741,6 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             acc[h][16 + i] = ffma2(s2, make_float2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1])),
-                                                   acc[h][16 + i]);
-                    } else {
-                        // one 32-column load at a time (registers hold the 128
-                        // accumulators); three P buffers give the two round
-                        // trips two steps of MMA time
-                        uint32_t v[32];
-                        tc_ld32(base, v);
-                        tc_wait_ld();
-                        tc_regs_ready(v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                              acc[h][i]);
-                        tc_ld32(base + 32, v);
-                        tc_wait_ld();
-                        tc_regs_ready(v);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&pfree[b]);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[h][16 + i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
                                                    acc[h][16 + i]);
                     }
                 }

@@ -100,6 +100,7 @@ struct Geo {
     static constexpr int MISC_OFF = SC_OFF + SC_RING * BM * 4;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;    // + slack to align the base
     static_assert(NS >= NA, "A stages are recycled through the X stage barriers");
+    static_assert(NA % 2 == 0, "a unit pair starting at an even unit owns two adjacent A stages");
     static_assert(BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_COL + 32 * NA <= TMEM_COLS, "tensor memory budget");
     // the dequant stores the scale of unit u + 1 once the MMAs of unit u - 1 -
@@ -149,25 +150,28 @@ __device__ __forceinline__ int range_cta(long long U, int grid, long long u) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D(tmem) (+)= A(tmem) . B(smem desc)^T, bf16 inputs, fp32 accumulate, issued
-// by one lane of a converged warp that the instruction itself elects (a
-// predicate, not a branch around the instruction).
-__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool accum) {
+// One 64-column group of one step: D(tmem) = A(tmem) . B(smem)^T as four
+// K = 16 MMAs (bf16 inputs, fp32 accumulate; the first overwrites D), then
+// commits of their completion to two mbarriers.  One elected lane of a
+// converged warp issues all six instructions under one predicate, with the
+// operand addresses precomputed: a warp issuing this way keeps the tensor pipe
+// busy (one M128 N128 K16 MMA per 64 cycles measured), where computing each
+// descriptor and electing per instruction took about 100 cycles per MMA.
+// a: A's tensor-memory address (K advances 8 columns per MMA); bd: B's
+// shared-memory descriptor (K advances 32 bytes, 2 in its address field).
+__device__ __forceinline__ void tc_mma_group(uint32_t d, uint32_t a, uint64_t bd, uint32_t idesc, uint64_t *bar0,
+                                             uint64_t *bar1) {
     asm volatile(
-        "{.reg .pred e, p; elect.sync _|e, 0xffffffff; setp.ne.u32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
-        ::"r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(accum ? 1u : 0u) : "memory");
+        "{.reg .pred e, z; elect.sync _|e, 0xffffffff; setp.ne.u32 z, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, z;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %5, %3, 1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %7, %3, 1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %9, %3, 1;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];}"
+        ::"r"(d), "r"(a), "l"(bd), "r"(idesc), "r"(a + 8), "l"(bd + 2), "r"(a + 16), "l"(bd + 4), "r"(a + 24),
+          "l"(bd + 6), "r"(smem_u32(bar0)), "r"(smem_u32(bar1)) : "memory");
 }
-
-// Commits of all previously issued MMAs of the elected lane to two mbarriers.
-__device__ __forceinline__ void tc_commit2_elect(uint64_t *bar0, uint64_t *bar1) {
-    asm volatile(
-        "{.reg .pred e; elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];}"
-        ::"r"(smem_u32(bar0)), "r"(smem_u32(bar1)) : "memory");
-}
-
 
 #define QG_R32(a) a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[8], a[9], a[10], a[11], a[12], a[13], a[14], \
                   a[15], a[16], a[17], a[18], a[19], a[20], a[21], a[22], a[23], a[24], a[25], a[26], a[27], a[28], \
@@ -182,6 +186,26 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// 64 consecutive columns in one load (columns 0..31 into r0, 32..63 into r1):
+// one tensor-memory instruction where two 32-column loads took two.
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]), "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]), "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31]),
+          "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]), "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]), "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]), "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+        : "r"(taddr));
+}
+
+// 64 consecutive columns in one store (r0 to columns 0..31, r1 to 32..63).
+__device__ __forceinline__ void tc_st64(uint32_t taddr, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+        :
+        : "r"(taddr), "r"(r0[0]), "r"(r0[1]), "r"(r0[2]), "r"(r0[3]), "r"(r0[4]), "r"(r0[5]), "r"(r0[6]), "r"(r0[7]), "r"(r0[8]), "r"(r0[9]), "r"(r0[10]), "r"(r0[11]), "r"(r0[12]), "r"(r0[13]), "r"(r0[14]), "r"(r0[15]), "r"(r0[16]), "r"(r0[17]), "r"(r0[18]), "r"(r0[19]), "r"(r0[20]), "r"(r0[21]), "r"(r0[22]), "r"(r0[23]), "r"(r0[24]), "r"(r0[25]), "r"(r0[26]), "r"(r0[27]), "r"(r0[28]), "r"(r0[29]), "r"(r0[30]), "r"(r0[31]),
+          "r"(r1[0]), "r"(r1[1]), "r"(r1[2]), "r"(r1[3]), "r"(r1[4]), "r"(r1[5]), "r"(r1[6]), "r"(r1[7]), "r"(r1[8]), "r"(r1[9]), "r"(r1[10]), "r"(r1[11]), "r"(r1[12]), "r"(r1[13]), "r"(r1[14]), "r"(r1[15]), "r"(r1[16]), "r"(r1[17]), "r"(r1[18]), "r"(r1[19]), "r"(r1[20]), "r"(r1[21]), "r"(r1[22]), "r"(r1[23]), "r"(r1[24]), "r"(r1[25]), "r"(r1[26]), "r"(r1[27]), "r"(r1[28]), "r"(r1[29]), "r"(r1[30]), "r"(r1[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -244,11 +268,11 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 }
 
 // Register budgets per warpgroup: the epilogue keeps up to 128 fp32
-// accumulators per thread and reads a split tile's partials beside them, so
-// the producer, MMA and dequant warps give registers up for it.  The block
+// accumulators per thread, with 64 loaded P values beside them, so the
+// producer, MMA and dequant warps give registers up for it.  The block
 // launches with 512 threads x 128 registers (65,536); the shares below add up
-// to at most 64,512 for every tile shape: 128 x (40 + 136) + 256 x 160
-// (128-token tiles), 128 x (40 + 96) + 256 x 184 (256), 128 x (40 + 144) +
+// to at most that for every tile shape: 128 x (40 + 136) + 256 x 160
+// (128-token tiles), 128 x (32 + 64) + 256 x 208 (256), 128 x (40 + 144) +
 // 256 x 152 (64).
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -266,8 +290,8 @@ __device__ __forceinline__ void regs_set() {
 // The 128-token tile's dequant decodes a pair of units at once (more
 // registers); the 256-token tile's epilogue holds twice the accumulators.
 template <int BH, int H> struct Regs {
-    static constexpr int WG0 = H == 2 ? 24 : 40;
-    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 72;
+    static constexpr int WG0 = H == 2 ? 32 : 40;
+    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 64;
     static constexpr int EPI = BH == 64 ? 152 : H == 1 ? 160 : 208;
     static_assert(128 * (WG0 + DQ) + 256 * EPI <= 512 * REGS_AT_LAUNCH, "register split");
 };
@@ -336,10 +360,13 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 // CODEC): pairs of units per weight stage; a unit's codes go into A stage
 // gi mod NA once the MMAs of unit gi - NA have freed it.  PAIR: both units of
 // a stage are decoded before either is stored, so that one store wait serves
-// two units (the integer codecs on the 128-token tile, where a unit's MMAs
-// are short); otherwise one unit at a time (fewer live registers: the FP8
-// decode, the 256-token tile's accumulators).
-template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR>
+// two units (the integer codecs on the 64- and 128-token tiles, where a unit's
+// MMAs are short); otherwise one unit at a time (fewer live registers: the FP8
+// decode, the 256-token tile's accumulators).  ST64: a pair starting at an
+// even unit is stored with one 64-column instruction (its two A stages are
+// adjacent); the kernels that also decode FP8 keep two 32-column stores, which
+// need fewer registers.
+template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR, bool ST64>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
                                                 float *sc_ring, uint32_t tmem, int q, int lane, float ts,
@@ -372,8 +399,13 @@ __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp
             }
             if (!ok) return false;
             tc_fence_after();
-            tc_st32(tmem + tlane + A_COL + (gi % NA) * 32, av[0]);
-            if (n == 2) tc_st32(tmem + tlane + A_COL + ((gi + 1) % NA) * 32, av[1]);
+            if (ST64 && n == 2 && (gi & 1) == 0) {
+                // stages gi mod NA and the next one are adjacent (NA is even)
+                tc_st64(tmem + tlane + A_COL + (gi % NA) * 32, av[0], av[1]);
+            } else {
+                tc_st32(tmem + tlane + A_COL + (gi % NA) * 32, av[0]);
+                if (n == 2) tc_st32(tmem + tlane + A_COL + ((gi + 1) % NA) * 32, av[1]);
+            }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -633,12 +665,8 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + P_COL + b * BH;
                 const uint32_t a = tmem + A_COL + (gi % NA) * 32;
-                const uint32_t b0 = smem_u32(xs + s * XST + h * HALF_BYTES);
-                // one lane elected by each instruction (predicated, no branch)
-#pragma unroll
-                for (int kk = 0; kk < GROUP / 16; ++kk)
-                    tc_mma_ts_elect(d, a + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, kk > 0);
-                tc_commit2_elect(&pfull[b], &xa_empty[s]);
+                tc_mma_group(d, a, smem_desc_sw128(smem_u32(xs + s * XST + h * HALF_BYTES)), idesc, &pfull[b],
+                             &xa_empty[s]);
                 __syncwarp();
                 last = j;
             }
@@ -661,17 +689,17 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const int codec = P.codec;
             const float ts = P.tscale;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             else if (F8 && codec == NVFP4)
-                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                           xa_empty, sc_ring, tmem, q, lane, ts,
                                                                           args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             else
-                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, lane, ts, args.status);
             u += k1 - k0;
         }
@@ -726,8 +754,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                         // both loads in flight before one wait: the buffer is
                         // released one load latency after it filled
                         uint32_t v0[32], v1[32];
-                        tc_ld32(base, v0);
-                        tc_ld32(base + 32, v1);
+                        tc_ld64(base, v0, v1);
                         tc_wait_ld();
                         tc_regs_ready(v0);
                         tc_regs_ready(v1);

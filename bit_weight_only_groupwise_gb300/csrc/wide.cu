@@ -508,6 +508,12 @@ __device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, i
     }
 }
 
+// Partial-sum slots of split tiles hold float4 groups of 4 consecutive tokens,
+// [BN / 4][BM] of them: element (token t, row r) at float4 (t / 4) BM + r,
+// component t mod 4, so that the 32 lanes of a warp (32 consecutive rows)
+// move 512 contiguous bytes per 16-byte access.
+__device__ __forceinline__ size_t part_q(int t, int r) { return (size_t)(t >> 2) * wide::BM + r; }
+
 // The sum of a split tile's partials, for one epilogue thread (row r, its
 // 64-token column block c of each half): every segment's partial, this CTA's
 // own included, is read back from the workspace and summed over the
@@ -525,22 +531,28 @@ __device__ __forceinline__ void fixup_sum(float2 (&acc)[H][NJ], const float *par
         for (int jb = 0; jb < NJ; jb += CH) {
             // a CTA's first segment sits in its slot 0, its last in slot 1
             auto seg = [&](int cc) {
-                return part + (size_t)(cc * 2 + (range_lo(U, grid, cc) >= u0 ? 0 : 1)) * BN * BM +
-                       (size_t)(h * BH + EW * c + 2 * jb) * BM + r;
+                return reinterpret_cast<const float4 *>(part + (size_t)(cc * 2 + (range_lo(U, grid, cc) >= u0 ? 0 : 1)) *
+                                                                   BN * BM) +
+                       part_q(h * BH + EW * c + 2 * jb, r);
             };
-            const float *p0 = seg(c_first);
+            const float4 *p0 = seg(c_first);
 #pragma unroll
-            for (int j = 0; j < CH; ++j)
-                acc[h][jb + j] = make_float2(__ldcg(p0 + (size_t)(2 * j) * BM), __ldcg(p0 + (size_t)(2 * j + 1) * BM));
+            for (int j = 0; j < CH; j += 2) {
+                const float4 x = __ldcg(p0 + (size_t)(j / 2) * BM);
+                acc[h][jb + j] = make_float2(x.x, x.y);
+                acc[h][jb + j + 1] = make_float2(x.z, x.w);
+            }
             for (int cc = c_first + 1; cc <= c_last; ++cc) {
-                const float *pc = seg(cc);
-                float2 v[CH];
+                const float4 *pc = seg(cc);
+                float4 v[CH / 2];
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    v[j] = make_float2(__ldcg(pc + (size_t)(2 * j) * BM), __ldcg(pc + (size_t)(2 * j + 1) * BM));
+                for (int j = 0; j < CH / 2; ++j) v[j] = __ldcg(pc + (size_t)j * BM);
 #pragma unroll
-                for (int j = 0; j < CH; ++j)
-                    acc[h][jb + j] = make_float2(acc[h][jb + j].x + v[j].x, acc[h][jb + j].y + v[j].y);
+                for (int j = 0; j < CH / 2; ++j) {
+                    acc[h][jb + 2 * j] = make_float2(acc[h][jb + 2 * j].x + v[j].x, acc[h][jb + 2 * j].y + v[j].y);
+                    acc[h][jb + 2 * j + 1] =
+                        make_float2(acc[h][jb + 2 * j + 1].x + v[j].z, acc[h][jb + 2 * j + 1].y + v[j].w);
+                }
             }
         }
 }
@@ -784,15 +796,13 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 const long long u0 = (long long)tile * G;
                 const int c_first = range_cta(U, gridDim.x, u0), c_last = range_cta(U, gridDim.x, u0 + G - 1);
                 // a CTA's first segment goes to its slot 0, its last to slot 1
-                float *mine = args.part + (size_t)(blockIdx.x * 2 + (lo >= u0 ? 0 : 1)) * BN * BM;
+                float4 *mine = reinterpret_cast<float4 *>(args.part + (size_t)(blockIdx.x * 2 + (lo >= u0 ? 0 : 1)) * BN * BM);
 #pragma unroll
                 for (int h = 0; h < H; ++h)
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j) {
-                        const int t = h * BH + EW * c + 2 * j;
-                        mine[(size_t)t * BM + r] = acc[h][j].x;
-                        mine[(size_t)(t + 1) * BM + r] = acc[h][j].y;
-                    }
+                    for (int j = 0; j < NJ; j += 2)
+                        mine[part_q(h * BH + EW * c + 2 * j, r)] =
+                            make_float4(acc[h][j].x, acc[h][j].y, acc[h][j + 1].x, acc[h][j + 1].y);
                 __threadfence();
                 __syncwarp();
                 unsigned int *cnt = tr.P->cnt + (size_t)tr.local * EPI_WARPS + e;

@@ -118,7 +118,7 @@ struct WideArgs {
     int ntt;              // token tiles of BN tokens
     int ntiles;           // output tiles of all parents (parent i owns p[i].cta_begin ...)
     long long units;      // ntiles * G
-    float *part;          // partial sums of split tiles: [grid][2][BN][BM]
+    float *part;          // partial sums of split tiles: [grid][2][BN / 4][BM] float4
     unsigned int *status;
 };
 

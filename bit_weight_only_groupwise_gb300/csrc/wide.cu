@@ -61,10 +61,10 @@ namespace qg {
 namespace wide {
 
 constexpr int BM = 128;                   // weight rows per tile (tensor-memory lanes)
-constexpr int DQ_WARPS = 4;               // one dequant warp per tensor-memory lane quarter
-constexpr int EPI_WARPS = 8;              // two epilogue warps per lane quarter (column halves)
-constexpr int DQ0 = 4, EPI0 = DQ0 + DQ_WARPS;
-constexpr int THREADS = (EPI0 + EPI_WARPS) * 32;
+constexpr int DQ_WARPS = 4;               // dequant warps of a unit: one per tensor-memory lane quarter
+constexpr int EPI_WARPS = 8;              // at most: two epilogue warps per lane quarter (column halves)
+constexpr int DQ0 = 4;                    // the first dequant warp (warps 0..3: producers, MMA issuers)
+constexpr int THREADS = 16 * 32;
 constexpr int SC_RING = 16;               // units of scales in flight
 constexpr int P_COL = 0;                  // P buffers from column 0, then the A stages
 constexpr int TMEM_COLS = 512;
@@ -80,10 +80,17 @@ constexpr int TMEM_COLS = 512;
 template <int BH_, int H, bool F8>
 struct Geo {
     static constexpr int BH = BH_;
+    // Warps 4 .. 15: DQG groups of four dequant warps (a group decodes every
+    // DQG-th unit pair) and EW_N epilogue warps.  The 64-token tile, limited
+    // by its dequant, runs two groups beside four epilogue warps that read
+    // all 64 columns of a step; the others one group beside eight.
+    static constexpr int DQG = BH == 64 ? 2 : 1;
+    static constexpr int EPI_N = 12 - 4 * DQG;
+    static constexpr int EPI_0 = DQ0 + 4 * DQG;
     static constexpr int NA = BH == 64 ? 8 : 4;           // A stages (unit u uses u mod NA)
     static constexpr int NP = (TMEM_COLS - 32 * NA) / BH;  // P buffers (step j uses j mod NP)
     static constexpr int A_COL = P_COL + NP * BH;         // A stages: 32 columns each
-    static constexpr int EW = BH / 2;                     // P columns per epilogue warp
+    static constexpr int EW = BH / (EPI_N / 4);           // P columns per epilogue warp
     static constexpr int NJ = EW / 2;                     // column pairs per epilogue thread and MMA
     static constexpr int HALF_BYTES = BH * GROUP * 2;     // one MMA's X tile of one group
     static constexpr int BN = H * BH;
@@ -107,6 +114,8 @@ struct Geo {
     // NA are done, and those waited for the epilogue of NP steps earlier
     static_assert(SC_RING >= NA + NP + 2, "scale ring shorter than the dequant lead");
     static_assert(BH == 64 || BH == 128, "MMA widths of the route");
+    static_assert(EPI_N % 4 == 0 && EPI_N <= EPI_WARPS, "whole lane quarters of epilogue warps");
+    static_assert(DQG == 1 || NWP % 2 == 0, "each group's weight stages reuse its own slots");
 };
 
 }  // namespace wide
@@ -272,8 +281,8 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // producer, MMA and dequant warps give registers up for it.  The block
 // launches with 512 threads x 128 registers (65,536); the shares below add up
 // to at most that for every tile shape: 128 x (40 + 136) + 256 x 160
-// (128-token tiles), 128 x (32 + 64) + 256 x 208 (256), 128 x (40 + 144) +
-// 256 x 152 (64).
+// (128-token tiles), 128 x (32 + 64) + 256 x 208 (256), 128 x 40 + 256 x 152
+// + 128 x 160 (64: two dequant groups, four epilogue warps).
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 template <int N>
@@ -291,9 +300,10 @@ __device__ __forceinline__ void regs_set() {
 // registers); the 256-token tile's epilogue holds twice the accumulators.
 template <int BH, int H> struct Regs {
     static constexpr int WG0 = H == 2 ? 32 : 40;
-    static constexpr int DQ = BH == 64 ? 144 : H == 1 ? 136 : 64;
-    static constexpr int EPI = BH == 64 ? 152 : H == 1 ? 160 : 208;
-    static_assert(128 * (WG0 + DQ) + 256 * EPI <= 512 * REGS_AT_LAUNCH, "register split");
+    static constexpr int DQ = BH == 64 ? 152 : H == 1 ? 136 : 64;
+    static constexpr int EPI = BH == 64 ? 160 : H == 1 ? 160 : 208;
+    static constexpr int DQG = wide::Geo<BH, H, false>::DQG, EPI_N = wide::Geo<BH, H, false>::EPI_N;
+    static_assert(128 * WG0 + 128 * DQG * DQ + 32 * EPI_N * EPI <= 512 * REGS_AT_LAUNCH, "register split");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -366,18 +376,22 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 // even unit is stored with one 64-column instruction (its two A stages are
 // adjacent); the kernels that also decode FP8 keep two 32-column stores, which
 // need fewer registers.
-template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR, bool ST64>
+template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR, bool ST64, int DQG>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
-                                                float *sc_ring, uint32_t tmem, int q, int lane, float ts,
+                                                float *sc_ring, uint32_t tmem, int q, int g, int lane, float ts,
                                                 unsigned int *status) {
     using namespace wide;
     constexpr int UB = unit_bytes(CODEC);
     const int r = q * 32 + lane;
     const uint32_t tlane = (uint32_t)(q * 32) << 16;
     for (int k = k0; k < k1; k += 2, ++jp) {
-        const int wsl = jp % NWP;
         const int n = k + 1 < k1 ? 2 : 1;
+        if (DQG > 1 && jp % DQG != g) {                   // another group's weight stage
+            gi += n;
+            continue;
+        }
+        const int wsl = jp % NWP;
         if (!mbar_wait_warp(&w_full[wsl], (jp / NWP) & 1, status)) return false;
         if constexpr (PAIR) {
             uint32_t av[2][32];
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NWP; ++i) { mbar_init(&w_full[i], 1); mbar_init(&w_empty[i], DQ_WARPS); }
         for (int i = 0; i < NS; ++i) { mbar_init(&xa_full[i], DQ_WARPS + 1); mbar_init(&xa_empty[i], H); }
-        for (int i = 0; i < NP; ++i) { mbar_init(&pfull[i], 1); mbar_init(&pfree[i], EPI_WARPS); }
+        for (int i = 0; i < NP; ++i) { mbar_init(&pfull[i], 1); mbar_init(&pfree[i], Gm::EPI_N); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -688,10 +702,11 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                 if (last >= 0) mbar_wait_limit(&pfull[last % NP], (last / NP) & 1, args.status, 64);
             }
         }
-    } else if (warp < EPI0) {
+    } else if (warp < Gm::EPI_0) {
         // ---------------- dequant: thread = weight row of the tile
         regs_set<Regs<BH, H>::DQ>();
         const int q = warp & 3;                           // tensor-memory lane quarter
+        const int g = (warp - DQ0) >> 2;                  // dequant group
         bool ok = true;
         int gi = 0, jp = 0;
         for (long long u = lo; u < hi && ok;) {
@@ -701,18 +716,18 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const int codec = P.codec;
             const float ts = P.tscale;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
-                                                                      xa_empty, sc_ring, tmem, q, lane, ts, args.status);
+                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                      xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             else if (F8 && codec == NVFP4)
-                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false, false>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
-                                                                          xa_empty, sc_ring, tmem, q, lane, ts,
+                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                          xa_empty, sc_ring, tmem, q, g, lane, ts,
                                                                           args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
-                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
+                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                       xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             else
-                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
-                                                                       xa_empty, sc_ring, tmem, q, lane, ts, args.status);
+                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                                                                       xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             u += k1 - k0;
         }
         if (!ok && lane == 0) *abort_flag = 1;
@@ -721,7 +736,7 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
         // [64 c, 64 c + 64) of each 128-token half
         regs_set<Regs<BH, H>::EPI>();
         pdl_wait_prior();                                 // Y, R and the workspace follow the previous kernel
-        const int q = warp & 3, c = (warp - EPI0) >> 2, e = warp - EPI0;
+        const int q = warp & 3, c = (warp - Gm::EPI_0) >> 2, e = warp - Gm::EPI_0;
         const int r = q * 32 + lane;
         const uint32_t tl = (uint32_t)(q * 32) << 16;
         bool ok = true;
@@ -749,22 +764,10 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                     const float sc = sc_ring[(gi % SC_RING) * BM + r];
                     const float2 s2 = make_float2(sc, sc);
                     const uint32_t base = tmem + tl + P_COL + b * BH + EW * c;
-                    if constexpr (EW == 32) {
-                        // one 32-column load per step
-                        uint32_t v[32];
-                        tc_ld32(base, v);
-                        tc_wait_ld();
-                        tc_regs_ready(v);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&pfree[b]);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                              acc[h][i]);
-                    } else {
-                        // both loads in flight before one wait: the buffer is
-                        // released one load latency after it filled
+                    {
+                        static_assert(EW == 64, "one 64-column load per warp and step");
+                        // the buffer is released one load latency after it
+                        // filled, before the rescale
                         uint32_t v0[32], v1[32];
                         tc_ld64(base, v0, v1);
                         tc_wait_ld();

@@ -34,19 +34,23 @@
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
 //                 a group (magic-number bf16 decode, exact) into tensor memory
 //                 as the A operand (tcgen05.st); the row's scale goes to the
-//                 epilogue through a shared-memory ring;
+//                 epilogue through a shared-memory ring (the 64-token tile:
+//                 warps 4..11, two groups taking alternate unit pairs);
 //   warps 8..15   epilogue: read P from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
-//                 (packed f32x2 FMA); write Y, or a partial sum and its count.
-// A step is one 128-token half of one group: step j = unit * H + h.
+//                 (packed f32x2 FMA); write Y, or a partial sum and its count
+//                 (the 64-token tile: warps 12..15, 64 columns each).
+// A step is one MMA width (128 tokens, or 64) of one group: step j = unit * H
+// + h.
 // Tensor memory: NA A stages of 32 columns (4; 8 for the 64-token tile) and
 // NP P buffers of 128 or 64 columns in the rest (step j uses j mod NP, so the
 // epilogue has NP - 1 steps of MMA time to drain a buffer).  Barriers:
-//   xa_full[s]   A_g stored (4 dequant warps) and X_g landed (TMA bytes)
+//   xa_full[s]   A_g stored (the 4 dequant warps of a group) and X_g landed
+//                (TMA bytes)
 //   xa_empty[s]  the MMAs of both halves of group g completed (one commit
 //                per step): X stage s and A stage g mod NA are free
 //   pfull[b]     the MMAs of the step in P buffer b completed
-//   pfree[b]     the 8 epilogue warps have read P buffer b
+//   pfree[b]     every epilogue warp has read P buffer b
 // Every mbarrier wait is bounded; a wait that runs out sets the device status
 // to timeout and the CTA winds down (after a bounded pause that lets copies
 // and MMAs already issued land before tensor memory is released).

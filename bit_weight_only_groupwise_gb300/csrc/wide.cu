@@ -913,6 +913,15 @@ static cudaError_t launch_t(const WideArgs &a, const CUtensorMap &xmap, int grid
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
+        // setmaxnreg moves each warpgroup from the launch's register count
+        // (REGS_AT_LAUNCH) to its share, raising or lowering it as regs_set
+        // decided at compile time; a kernel built with any other count would
+        // run a lowering that raises (an illegal instruction), so it is never
+        // launched
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, wide_kernel<BH, H, FUSED, F8>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != REGS_AT_LAUNCH) return cudaErrorInvalidKernelImage;
         e = cudaFuncSetAttribute(wide_kernel<BH, H, FUSED, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);

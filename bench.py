@@ -433,10 +433,9 @@ class Config:
             raise qg.QgemmError(st, "run")
 
     def launches(self, T) -> int:
-        """Kernels one call at width T launches (the tcgen05 route runs one
-        launch per codec among a call's parents)."""
-        if self.sets[0][0].route(T).startswith("tcgen05"):
-            return len({w.codec for w in self.sets[0]})
+        """Kernels one call at width T launches: one on every route (the
+        parents of a multi-parent call share one launch, whatever their
+        codecs)."""
         return 1
 
 
@@ -589,21 +588,41 @@ def run_ours(args, desc):
         h2d = sum(h.numel() * 2 for h in hx.values()) + sum(h.numel() * 4 for h in hr.values())
         d2h = sum(y.numel() * 4 for ys in hy.values() for y in ys)
         e_steps = max(1, min(args.steps, args.e2e_steps))
+        # three streams: the upload of a call's X (and residual), the call
+        # itself, the download of its Y; each waits for the stage before it
+        # (events), so one call's copies overlap the next calls' work.  Every
+        # call has its own device and pinned host buffers.
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        downloaded = {}                   # call -> event: its Y is on the host (its buffers are free)
         for i in range(e_steps):
             for ci, c, T in calls(desc):
                 k = (ci, T)
-                dx[k].copy_(hx[k], non_blocking=True)
-                if k in hr:
-                    dr[k].copy_(hr[k], non_blocking=True)
-                cfgs[ci].call(qg, torch, i, T, X=dx[k], Rt=dr.get(k))
-                for y, h in zip(cfgs[ci].ys[T], hy[k]):
-                    h.copy_(y, non_blocking=True)
-            stream.synchronize()          # the step's results are on the host
+                with torch.cuda.stream(up):
+                    if k in downloaded:
+                        up.wait_event(downloaded[k])
+                    dx[k].copy_(hx[k], non_blocking=True)
+                    if k in hr:
+                        dr[k].copy_(hr[k], non_blocking=True)
+                    landed = torch.cuda.Event()
+                    landed.record(up)
+                stream.wait_event(landed)
+                with torch.cuda.stream(stream):
+                    cfgs[ci].call(qg, torch, i, T, X=dx[k], Rt=dr.get(k))
+                    done = torch.cuda.Event()
+                    done.record(stream)
+                down.wait_event(done)
+                with torch.cuda.stream(down):
+                    for y, h in zip(cfgs[ci].ys[T], hy[k]):
+                        h.copy_(y, non_blocking=True)
+                    downloaded[k] = torch.cuda.Event()
+                    downloaded[k].record(down)
+            down.synchronize()            # the step's results are on the host
+        stream.wait_stream(down)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(max(e0.elapsed_time(e1), 1e3 * (time.perf_counter() - t0)), world)

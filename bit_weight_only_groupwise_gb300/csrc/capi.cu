@@ -37,38 +37,44 @@ enum Route : int {
     ROUTE_SKINNY32 = 2,    // 32-token tile
     ROUTE_WIDE128 = 3,     // stream-K tcgen05 tiles of 128 rows x 128 tokens
     ROUTE_WIDE256 = 4,     // stream-K tcgen05 tiles of 128 rows x 256 tokens (two 128-token halves)
-    ROUTE_WIDE64 = 5,      // stream-K tcgen05 tiles of 128 rows x 64 tokens (six P buffers)
+    ROUTE_WIDE64 = 5,      // stream-K tcgen05 tiles of 128 rows x 64 tokens
+    ROUTE_WIDE32 = 6,      // stream-K tcgen05 tiles of 128 rows x 32 tokens
     ROUTE_COUNT
 };
 
 static const char *kRouteNames[ROUTE_COUNT] = {"skinny8", "skinny16", "skinny32", "tcgen05_128x128",
-                                               "tcgen05_128x256", "tcgen05_128x64"};
+                                               "tcgen05_128x256", "tcgen05_128x64", "tcgen05_128x32"};
 
 static int route_tokens(int route) {
     switch (route) {
         case ROUTE_SKINNY8: return 8;
         case ROUTE_SKINNY16: return 16;
         case ROUTE_SKINNY32: return 32;
+        case ROUTE_WIDE32: return 32;
         case ROUTE_WIDE64: return 64;
         case ROUTE_WIDE128: return 128;
         default: return 256;
     }
 }
 
-static bool wide_route(int route) { return route == ROUTE_WIDE64 || route == ROUTE_WIDE128 || route == ROUTE_WIDE256; }
+static bool wide_route(int route) {
+    return route == ROUTE_WIDE32 || route == ROUTE_WIDE64 || route == ROUTE_WIDE128 || route == ROUTE_WIDE256;
+}
 
 // The route table, from per-T sweeps with every route forced on the pages'
 // projection shapes (5120 x 6144, 7168 x 5120, 12288 x 5120; cold weights):
 // the narrowest tile that covers T (the padded width sets the cost, not the
-// live column count), except that the 64-token tcgen05 tile beats the
-// 32-token small-T tile from T = 17 on, and that above 128 tokens the
-// 256-token tile pays only from 512 tokens, or from 129 when the launch has
-// at least 96 row blocks of 128 (enough tiles to fill the GPU either way).
+// live column count), except that the tcgen05 tiles beat the 32-token
+// small-T tile from T = 17 on (the 32-token one to T = 32, 12-16% ahead of
+// the 64-token one there), and that above 128 tokens the 256-token tile pays
+// only from 512 tokens, or from 129 when the launch has at least 96 row
+// blocks of 128 (enough tiles to fill the GPU either way).
 // nb: the launch's 128-row blocks, summed over its parents.  A route forced
 // on the plan (qgemm_plan_force_route) takes every T its token tile covers.
 static int table_route(int T, int nb) {
     if (T <= 8) return ROUTE_SKINNY8;
     if (T <= 16) return ROUTE_SKINNY16;
+    if (T <= 32) return ROUTE_WIDE32;
     if (T <= 64) return ROUTE_WIDE64;
     if (T <= 128) return ROUTE_WIDE128;
     return (T >= 512 || nb >= 96) ? ROUTE_WIDE256 : ROUTE_WIDE128;
@@ -367,7 +373,8 @@ static qgemm_status run_parents(const qgemm_plan_s *const *plans, int np, const 
             wp[i].ybf16 = plans[i]->out == QGEMM_OUT_BF16;
         }
         // the partial-sum slots of the first parent's workspace serve the launch
-        if (launch_wide(wp, np, X, T, K, route == ROUTE_WIDE64 ? 64 : 128, route == ROUTE_WIDE256 ? 2 : 1,
+        if (launch_wide(wp, np, X, T, K, route == ROUTE_WIDE32 ? 32 : route == ROUTE_WIDE64 ? 64 : 128,
+                        route == ROUTE_WIDE256 ? 2 : 1,
                         reinterpret_cast<float *>(plans[0]->ws), status, pdl, plans[0]->sms, stream) != cudaSuccess)
             return QGEMM_ERR_CUDA;
         g_launches.fetch_add(1);

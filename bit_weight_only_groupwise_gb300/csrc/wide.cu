@@ -69,7 +69,6 @@ constexpr int DQ_WARPS = 4;               // dequant warps of a unit: one per te
 constexpr int EPI_WARPS = 8;              // at most: two epilogue warps per lane quarter (column halves)
 constexpr int DQ0 = 4;                    // the first dequant warp (warps 0..3: producers, MMA issuers)
 constexpr int THREADS = 16 * 32;
-constexpr int SC_RING = 16;               // units of scales in flight
 constexpr int P_COL = 0;                  // P buffers from column 0, then the A stages
 constexpr int TMEM_COLS = 512;
 
@@ -88,25 +87,33 @@ struct Geo {
     // DQG-th unit pair) and EW_N epilogue warps.  The 64-token tile, limited
     // by its dequant, runs two groups beside four epilogue warps that read
     // all 64 columns of a step; the others one group beside eight.
-    static constexpr int DQG = BH == 64 ? 2 : 1;
+    static constexpr int DQG = BH <= 64 ? 2 : 1;
     static constexpr int EPI_N = 12 - 4 * DQG;
     static constexpr int EPI_0 = DQ0 + 4 * DQG;
-    static constexpr int NA = BH == 64 ? 8 : 4;           // A stages (unit u uses u mod NA)
-    static constexpr int NP = (TMEM_COLS - 32 * NA) / BH;  // P buffers (step j uses j mod NP)
+    static constexpr int NA = BH <= 64 ? 8 : 4;           // A stages (unit u uses u mod NA)
+    // P buffers (step j uses j mod NP): as many as fit, at most 6 (the scale
+    // ring covers NA + NP + 2 units)
+    static constexpr int NP = (TMEM_COLS - 32 * NA) / BH < 6 ? (TMEM_COLS - 32 * NA) / BH : 6;
     static constexpr int A_COL = P_COL + NP * BH;         // A stages: 32 columns each
     static constexpr int EW = BH / (EPI_N / 4);           // P columns per epilogue warp
     static constexpr int NJ = EW / 2;                     // column pairs per epilogue thread and MMA
     static constexpr int HALF_BYTES = BH * GROUP * 2;     // one MMA's X tile of one group
     static constexpr int BN = H * BH;
     static constexpr int XST = H * HALF_BYTES;           // X stage: BN tokens x 64 columns
-    static constexpr int X_REGION = BH == 64 ? 64 * 1024 : 128 * 1024;  // activation stages
+    static constexpr int X_REGION = BH <= 64 ? 64 * 1024 : 128 * 1024;  // activation stages
     static constexpr int NS = X_REGION / XST;             // 8 (64- and 128-token tiles) or 4 stages
     static constexpr int WSLOT = 2 * (F8 ? UNIT8 : UNIT5);
-    static constexpr int NWP = BH == 64 ? (F8 ? 8 : 12) : (F8 ? 4 : 6);  // weight stages (pairs of units)
+    static constexpr int NWP = BH <= 64 ? (F8 ? 8 : 12) : (F8 ? 4 : 6);  // weight stages (pairs of units)
     static constexpr int X_OFF = 0;                       // 1024-aligned (128B swizzle atoms)
     static constexpr int W_OFF = X_REGION;
     static constexpr int BAR_OFF = W_OFF + NWP * WSLOT;
     static constexpr int NBAR = 2 * NWP + 2 * NS + 2 * NP;
+    // Scales in flight: the dequant writes unit u's scale while decoding it,
+    // before it waits for the MMAs of unit u - NA; a group's previous pair
+    // waited for those of its own units, which came after the epilogue had
+    // read NP steps earlier -- so a group writes up to NA + NP + 2 units past
+    // the epilogue, and DQG groups (alternate pairs) 2 (DQG - 1) more.
+    static constexpr int SC_RING = DQG > 1 ? 32 : 16;
     static constexpr int SC_OFF = BAR_OFF + NBAR * 8;     // float [SC_RING][BM]
     static constexpr int MISC_OFF = SC_OFF + SC_RING * BM * 4;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;    // + slack to align the base
@@ -114,10 +121,8 @@ struct Geo {
     static_assert(NA % 2 == 0, "a unit pair starting at an even unit owns two adjacent A stages");
     static_assert(BYTES <= 227 * 1024, "shared memory budget");
     static_assert(A_COL + 32 * NA <= TMEM_COLS, "tensor memory budget");
-    // the dequant stores the scale of unit u + 1 once the MMAs of unit u - 1 -
-    // NA are done, and those waited for the epilogue of NP steps earlier
-    static_assert(SC_RING >= NA + NP + 2, "scale ring shorter than the dequant lead");
-    static_assert(BH == 64 || BH == 128, "MMA widths of the route");
+    static_assert(SC_RING >= NA + NP + 2 * DQG, "scale ring shorter than the dequant lead");
+    static_assert(BH == 32 || BH == 64 || BH == 128, "MMA widths of the route");
     static_assert(EPI_N % 4 == 0 && EPI_N <= EPI_WARPS, "whole lane quarters of epilogue warps");
     static_assert(DQG == 1 || NWP % 2 == 0, "each group's weight stages reuse its own slots");
 };
@@ -303,9 +308,9 @@ __device__ __forceinline__ void regs_set() {
 // The 128-token tile's dequant decodes a pair of units at once (more
 // registers); the 256-token tile's epilogue holds twice the accumulators.
 template <int BH, int H> struct Regs {
-    static constexpr int WG0 = H == 2 ? 32 : 40;
-    static constexpr int DQ = BH == 64 ? 152 : H == 1 ? 136 : 64;
-    static constexpr int EPI = BH == 64 ? 160 : H == 1 ? 160 : 208;
+    static constexpr int WG0 = H == 2 ? 32 : 40;      // (the same for every BH <= 64)
+    static constexpr int DQ = BH <= 64 ? 152 : H == 1 ? 136 : 64;
+    static constexpr int EPI = BH <= 64 ? 160 : H == 1 ? 160 : 208;
     static constexpr int DQG = wide::Geo<BH, H, false>::DQG, EPI_N = wide::Geo<BH, H, false>::EPI_N;
     static_assert(128 * WG0 + 128 * DQG * DQ + 32 * EPI_N * EPI <= 512 * REGS_AT_LAUNCH, "register split");
 };
@@ -380,7 +385,7 @@ __device__ __forceinline__ float decode_row(const uint8_t *u, int r, uint32_t (&
 // even unit is stored with one 64-column instruction (its two A stages are
 // adjacent); the kernels that also decode FP8 keep two 32-column stores, which
 // need fewer registers.
-template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR, bool ST64, int DQG>
+template <int CODEC, int NS, int NA, int NWP, int WSLOT, int A_COL, bool PAIR, bool ST64, int DQG, int SC_RING>
 __device__ __forceinline__ bool dequant_segment(int k0, int k1, int &gi, int &jp, uint8_t *ws, uint64_t *w_full,
                                                 uint64_t *w_empty, uint64_t *xa_full, uint64_t *xa_empty,
                                                 float *sc_ring, uint32_t tmem, int q, int g, int lane, float ts,
@@ -720,17 +725,17 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             const int codec = P.codec;
             const float ts = P.tscale;
             if (F8 && codec == 8)
-                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<8, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG, Gm::SC_RING>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                       xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             else if (F8 && codec == NVFP4)
-                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<NVFP4, NS, NA, NWP, WSLOT, A_COL, false, false, Gm::DQG, Gm::SC_RING>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                           xa_empty, sc_ring, tmem, q, g, lane, ts,
                                                                           args.status);
             else if (codec == 5)
-                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<5, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG, Gm::SC_RING>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             else
-                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
+                ok = dequant_segment<4, NS, NA, NWP, WSLOT, A_COL, H == 1, !F8, Gm::DQG, Gm::SC_RING>(k0, k1, gi, jp, ws, w_full, w_empty, xa_full,
                                                                        xa_empty, sc_ring, tmem, q, g, lane, ts, args.status);
             u += k1 - k0;
         }
@@ -765,11 +770,23 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
                     tc_fence_after();
                     // the unit's scale (stored by the dequant before the MMAs
                     // of this step could start)
-                    const float sc = sc_ring[(gi % SC_RING) * BM + r];
+                    const float sc = sc_ring[(gi % Gm::SC_RING) * BM + r];
                     const float2 s2 = make_float2(sc, sc);
                     const uint32_t base = tmem + tl + P_COL + b * BH + EW * c;
-                    {
-                        static_assert(EW == 64, "one 64-column load per warp and step");
+                    if constexpr (EW == 32) {
+                        uint32_t v[32];
+                        tc_ld32(base, v);
+                        tc_wait_ld();
+                        tc_regs_ready(v);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&pfree[b]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[h][i] = ffma2(s2, make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                              acc[h][i]);
+                    } else {
+                        static_assert(EW == 64, "one 32- or 64-column load per warp and step");
                         // the buffer is released one load latency after it
                         // filled, before the rescale
                         uint32_t v0[32], v1[32];
@@ -890,8 +907,10 @@ constexpr int MIN_UNITS_PER_CTA = 8;
 // to T_max: the partial-sum slots of one launch (two per CTA, sized for the
 // widest token tile the plan's widths can take, wide_max_tokens) and the
 // plan's split-tile counters (eight per tile at the largest tile count any of
-// the route's widths gives, that of 64-token tiles).
-int wide_max_tokens(int T_max) { return T_max <= 16 ? 0 : T_max <= 64 ? 64 : T_max <= 128 ? 128 : 256; }
+// the route's widths gives, that of 32-token tiles).
+int wide_max_tokens(int T_max) {
+    return T_max <= 16 ? 0 : T_max <= 32 ? 32 : T_max <= 64 ? 64 : T_max <= 128 ? 128 : 256;
+}
 
 size_t wide_partial_bytes(int T_max, int sms) {
     return (size_t)sms * 2 * wide_max_tokens(T_max) * wide::BM * sizeof(float);
@@ -900,7 +919,7 @@ size_t wide_partial_bytes(int T_max, int sms) {
 size_t wide_workspace_bytes(int rows, int T_max, int sms) {
     if (wide_max_tokens(T_max) == 0) return 0;
     const int NB = (rows + wide::BM - 1) / wide::BM;
-    const size_t tiles = (size_t)NB * ((T_max + 63) / 64);
+    const size_t tiles = (size_t)NB * ((T_max + 31) / 32);
     return wide_partial_bytes(T_max, sms) + tiles * wide::EPI_WARPS * sizeof(unsigned int);
 }
 
@@ -955,7 +974,8 @@ static cudaError_t launch_h(const WideArgs &a, const CUtensorMap &xmap, int grid
 // each parent's cnt its zeroed counters.  At most `sms` CTAs.
 cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T, int K, int bh, int halves,
                         float *part, unsigned int *status, bool pdl, int sms, cudaStream_t stream) {
-    if (!((bh == 64 && halves == 1) || (bh == 128 && (halves == 1 || halves == 2)))) return cudaErrorInvalidValue;
+    if (!(((bh == 32 || bh == 64) && halves == 1) || (bh == 128 && (halves == 1 || halves == 2))))
+        return cudaErrorInvalidValue;
     const int BN = halves * bh;
     CUtensorMap xmap;
     cudaError_t e = make_xmap(&xmap, X, T, K, BN);
@@ -987,6 +1007,7 @@ cudaError_t launch_wide(const WideParent *parents, int np, const void *X, int T,
     long long grid = a.units / MIN_UNITS_PER_CTA;
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
+    if (bh == 32) return launch_h<32, 1>(a, xmap, (int)grid, fused, f8, pdl, stream);
     if (bh == 64) return launch_h<64, 1>(a, xmap, (int)grid, fused, f8, pdl, stream);
     return halves == 2 ? launch_h<128, 2>(a, xmap, (int)grid, fused, f8, pdl, stream)
                        : launch_h<128, 1>(a, xmap, (int)grid, fused, f8, pdl, stream);

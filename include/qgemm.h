@@ -148,9 +148,9 @@ qgemm_status qgemm_plan(int N, int K, qgemm_codec codec, int T_max, qgemm_plan_t
  * T_max <= 16 run on the small-T routes only and need none.  Above that the
  * tcgen05 routes split output tiles across CTAs (stream-K) and need, per
  * launch, two fp32 partial-sum slots per SM of the widest token tile the
- * plan's widths can take (64 tokens up to T_max = 64, 128 up to 128, else 256)
- * times 128 rows, plus eight 32-bit counters per 128-row block and 64-token
- * tile.  Passage: "ninfer-3080 docs/performance.md", token tile section (the
+ * plan's widths can take (32 tokens up to T_max = 32, 64 up to 64, 128 up to
+ * 128, else 256) times 128 rows, plus eight 32-bit counters per 128-row block
+ * and 32-token tile.  Passage: "ninfer-3080 docs/performance.md", token tile section (the
  * token tile sets the weight passes); the split and its workspace are this
  * library's, not the pages'. */
 size_t qgemm_plan_workspace_bytes(qgemm_plan_t plan);

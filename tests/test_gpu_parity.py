@@ -180,8 +180,8 @@ def test_one_route_per_call(T):
     launched = qg.qgemm_launch_count() - n0
     assert launched == 1, (route, launched)
     # 256 rows, 2 row blocks: the 128-token tile up to T = 511
-    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "tcgen05_128x64" if T <= 64
-                     else "tcgen05_128x128" if T < 512 else "tcgen05_128x256")
+    assert route == ("skinny8" if T <= 8 else "skinny16" if T <= 16 else "tcgen05_128x32" if T <= 32
+                     else "tcgen05_128x64" if T <= 64 else "tcgen05_128x128" if T < 512 else "tcgen05_128x256")
     n0 = qg.qgemm_launch_count()
     qg.GroupwiseWeights(4, 256, 512, p["packed"], p["scales"], T_max=8)
     assert qg.qgemm_launch_count() - n0 == 2            # pack + its ordering kernel

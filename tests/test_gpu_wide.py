@@ -21,7 +21,7 @@ qg = pytest.importorskip("bit_weight_only_groupwise_gb300")
 
 pytestmark = pytest.mark.gpu
 
-SKINNY16, SKINNY32, WIDE128, WIDE256, WIDE64 = 1, 2, 3, 4, 5
+SKINNY16, SKINNY32, WIDE128, WIDE256, WIDE64, WIDE32 = 1, 2, 3, 4, 5, 6
 
 
 @pytest.fixture(autouse=True)
@@ -53,7 +53,7 @@ def check(p, x, Y, what, cols=None):
 
 
 @pytest.mark.parametrize("N,K,T", [(256, 8192, 40), (130, 4096, 200), (1000, 1024, 129), (128, 64, 33)])
-@pytest.mark.parametrize("route", [WIDE64, WIDE128, WIDE256])
+@pytest.mark.parametrize("route", [WIDE32, WIDE64, WIDE128, WIDE256])
 def test_split_tiles_match_the_oracle(N, K, T, route):
     # few tiles and many groups: each tile is split over many CTAs
     p = synth.weights(40, N, K, 4)
@@ -92,7 +92,7 @@ def test_every_tile_width_agrees_with_the_oracle(bits):
     x = synth.activations(42, T, K, outliers=True)
     X = dev_x(x)
     cols = wide_columns(T)
-    for route in (WIDE64, WIDE128, WIDE256):
+    for route in (WIDE32, WIDE64, WIDE128, WIDE256):
         W = weights(p, T_max=T, route=route)
         check(p, x, W.run(X), f"int{bits} {W.route(T)}", cols=cols)
 
@@ -101,11 +101,12 @@ def test_forcing_a_wide_route_needs_its_workspace():
     p = synth.weights(43, 256, 512, 4)
     tiny = weights(p, T_max=16)
     assert qg.qgemm_plan_workspace_bytes(tiny.plan) == 0
-    assert qg.qgemm_plan_force_route(tiny.plan, WIDE64) == qg.QGEMM_ERR_INVALID_ARG
-    assert qg.qgemm_plan_force_route(tiny.plan, WIDE128) == qg.QGEMM_ERR_INVALID_ARG
+    for route in (WIDE32, WIDE64, WIDE128):
+        assert qg.qgemm_plan_force_route(tiny.plan, route) == qg.QGEMM_ERR_INVALID_ARG
     small = weights(p, T_max=32)
     assert qg.qgemm_plan_force_route(small.plan, WIDE128) == qg.QGEMM_ERR_INVALID_ARG
-    assert qg.qgemm_plan_force_route(small.plan, WIDE64) == qg.QGEMM_OK
+    assert qg.qgemm_plan_force_route(small.plan, WIDE64) == qg.QGEMM_ERR_INVALID_ARG
+    assert qg.qgemm_plan_force_route(small.plan, WIDE32) == qg.QGEMM_OK
     mid = weights(p, T_max=128)
     assert qg.qgemm_plan_force_route(mid.plan, WIDE256) == qg.QGEMM_ERR_INVALID_ARG
     assert qg.qgemm_plan_force_route(mid.plan, WIDE128) == qg.QGEMM_OK
@@ -135,12 +136,12 @@ def test_forced_small_t_tiles(bits, K, T):
 @pytest.mark.parametrize("T_max", [17, 32, 64])
 def test_table_route_within_a_narrow_domain(T_max):
     # a plan whose widths stop between 17 and 64 has the workspace of the
-    # 64-token tcgen05 tile the table picks for T > 16
+    # 32- and 64-token tcgen05 tiles the table picks for T = 17 .. 64
     N, K = 1000, 1024
     p = synth.weights(45, N, K, 4)
     W = weights(p, T_max=T_max)
     assert qg.qgemm_plan_workspace_bytes(W.plan) > 0
-    for T in sorted({17, T_max}):
+    for T in sorted(t for t in {17, 32, T_max} if t <= T_max):
         x = synth.activations(45 + T, T, K, outliers=True)
-        assert W.route(T) == "tcgen05_128x64"
+        assert W.route(T) == ("tcgen05_128x32" if T <= 32 else "tcgen05_128x64")
         check(p, x, W.run(dev_x(x)), f"T_max={T_max} T={T} {W.route(T)}")

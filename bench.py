@@ -591,37 +591,45 @@ def run_ours(args, desc):
         # three streams: the upload of a call's X (and residual), the call
         # itself, the download of its Y; each waits for the stage before it
         # (events), so one call's copies overlap the next calls' work.  Every
-        # call has its own device and pinned host buffers.
+        # call has its own device and pinned host buffers, and its own three
+        # events (landed, done, downloaded), recorded again every step: a wait
+        # takes the event as last recorded when the wait is issued.  The host
+        # consumes results one step behind: before it issues step i + 1, the
+        # results of step i - 1 are on the host, so at most two steps are in
+        # flight and every step's Y is read back inside the timed region.
         up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        evs = {k: (torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()) for k in hx}
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        downloaded = {}                   # call -> event: its Y is on the host (its buffers are free)
+        prev_step = None                  # event: the previous step's results are on the host
         for i in range(e_steps):
             for ci, c, T in calls(desc):
                 k = (ci, T)
+                landed, done, downloaded = evs[k]
                 with torch.cuda.stream(up):
-                    if k in downloaded:
-                        up.wait_event(downloaded[k])
+                    if i > 0:
+                        up.wait_event(downloaded)     # this call's buffers of the step before are free
                     dx[k].copy_(hx[k], non_blocking=True)
                     if k in hr:
                         dr[k].copy_(hr[k], non_blocking=True)
-                    landed = torch.cuda.Event()
                     landed.record(up)
                 stream.wait_event(landed)
                 with torch.cuda.stream(stream):
                     cfgs[ci].call(qg, torch, i, T, X=dx[k], Rt=dr.get(k))
-                    done = torch.cuda.Event()
                     done.record(stream)
                 down.wait_event(done)
                 with torch.cuda.stream(down):
                     for y, h in zip(cfgs[ci].ys[T], hy[k]):
                         h.copy_(y, non_blocking=True)
-                    downloaded[k] = torch.cuda.Event()
-                    downloaded[k].record(down)
-            down.synchronize()            # the step's results are on the host
+                    downloaded.record(down)
+            if prev_step is not None:
+                prev_step.synchronize()       # step i - 1's results are on the host
+            prev_step = torch.cuda.Event()
+            prev_step.record(down)
+        down.synchronize()                    # every step's results are on the host
         stream.wait_stream(down)
         e1.record(stream)
         torch.cuda.synchronize()

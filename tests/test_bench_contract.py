@@ -1,10 +1,12 @@
-"""bench.py's reference arm (the fp64 oracle on the host cores) on the CPU:
-one JSON line with the contract's keys, within its time budget."""
+"""bench.py's JSON line: the reference arm (the fp64 oracle on the host cores)
+on the CPU, within its time budget, and the timed arm on a GPU."""
 import json
 import os
 import subprocess
 import sys
 import time
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -23,3 +25,29 @@ def test_reference_arm_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"] == "all"
     assert time.time() - t0 < 120          # the budget, not the step count, sets the time
+
+
+@pytest.mark.gpu
+def test_bench_line_on_the_gpu():
+    """The timed arm on the decode workload: one JSON line with the contract's
+    keys, a live roofline of the dominant kernel, an end-to-end number that
+    moved bytes both ways, the oracle's CPU baseline and the sampled clocks."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "decode", "--steps", "10",
+                          "--warmup", "3", "--cpu-seconds", "1", "--e2e-steps", "3"],
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["steps"] == 10 and line["warmup"] == 3 and line["value"] > 0
+    assert line["config"]["workload"] == "decode"
+    roof = line["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and 0 < roof["frac"] < 1.5
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert e2e["value"] < line["value"]                 # the copies cost time
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] > 0
+    assert line["gpu_launches"] > 0
+    assert line["clocks"]["sm_max_mhz"] > 0

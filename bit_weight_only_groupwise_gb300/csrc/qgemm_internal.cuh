@@ -238,17 +238,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, u
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-// Bounded wait by a converged warp that polls with the non-blocking test
-// instead of suspending: for a warp whose wait is on the critical path and
-// usually short, the wake-up of a suspended warp measured later than polling.
-// About SPIN_LIMIT * 1024 tests at most.
-__device__ __forceinline__ bool mbar_spin_warp(uint64_t *bar, uint32_t parity, unsigned int *status) {
-    for (long long i = 0; i < SPIN_LIMIT * 1024; ++i)
-        if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-    atomicExch(status, 7u /* QGEMM_ERR_TIMEOUT */);
-    return false;
-}
-
 // 16-byte asynchronous global -> shared copy (L2 only), committed in groups.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");

@@ -34,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -156,20 +157,31 @@ def route_kernel(route: str, K: int) -> tuple:
     return ("qg::skinny_line_kernel" if full else "qg::skinny_kernel"), "skinny.cu"
 
 
+def kernel_code_sha256(path: str) -> str:
+    """sha256 of a kernel source's code: comments removed and runs of
+    whitespace collapsed, so that an edit of comments alone keeps the hash
+    (the kernel's instructions, and so its DRAM traffic, are unchanged) and
+    any change of code does not."""
+    src = open(path, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()
+
+
 def recorded_traffic(kernel_src: str, profile_name: str, keys):
     """Mean per-launch DRAM bytes over the calls `keys` ("config:T") from a
-    committed ncu summary, if it was taken on this kernel source and covers
+    committed ncu summary, if it was taken on this kernel's code and covers
     every one of them; else None."""
     path = os.path.join(PROFILES, profile_name)
     if not os.path.exists(path):
         return None
-    want = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    want = kernel_code_sha256(kernel_src)
     rec = {}
     for line in open(path):
         if ":" in line:
             k, v = line.split(":", 1)
             rec[k.strip().lstrip("-* ")] = v.strip()
-    if rec.get("kernel_source_sha256") != want:
+    if rec.get("kernel_code_sha256") != want:
         return None
     try:
         by_call = json.loads(rec["dram_bytes_by_call"])

@@ -6,7 +6,7 @@
 // docs/performance.md", token tile section: the token tile width sets how
 // often the weights are re-streamed, and the per-group rescale and the operand
 // assembly are the costs beside the MMAs).  An output tile is 128 weight rows
-// by BN = 128 or 256 tokens:
+// by BN = 32, 64, 128 or 256 tokens:
 //
 //   D[128 rows x BN tokens] = sum over 64-column groups g of s[:, g] * P_g,
 //   P_g = A_g (exact integer codes as bf16, 128 x 64) . B_g (X tile, BN x 64)^T
@@ -34,17 +34,19 @@
 //   warps 4..7    dequant: one thread per weight row decodes its 64 codes of
 //                 a group (magic-number bf16 decode, exact) into tensor memory
 //                 as the A operand (tcgen05.st); the row's scale goes to the
-//                 epilogue through a shared-memory ring (the 64-token tile:
-//                 warps 4..11, two groups taking alternate unit pairs);
+//                 epilogue through a shared-memory ring (the 32- and
+//                 64-token tiles: warps 4..11, two groups taking alternate
+//                 unit pairs);
 //   warps 8..15   epilogue: read P from tensor memory (tcgen05.ld), multiply
 //                 by the row's fp16 scale and accumulate in fp32 registers
 //                 (packed f32x2 FMA); write Y, or a partial sum and its count
-//                 (the 64-token tile: warps 12..15, 64 columns each).
-// A step is one MMA width (128 tokens, or 64) of one group: step j = unit * H
-// + h.
-// Tensor memory: NA A stages of 32 columns (4; 8 for the 64-token tile) and
-// NP P buffers of 128 or 64 columns in the rest (step j uses j mod NP, so the
-// epilogue has NP - 1 steps of MMA time to drain a buffer).  Barriers:
+//                 (the 32- and 64-token tiles: warps 12..15, 32 or 64 columns
+//                 each).
+// A step is one MMA width (BH = 128, 64 or 32 tokens) of one group: step
+// j = unit * H + h.
+// Tensor memory: NA A stages of 32 columns (4; 8 for the 32- and 64-token
+// tiles) and NP P buffers of BH columns in the rest (step j uses j mod NP, so
+// the epilogue has NP - 1 steps of MMA time to drain a buffer).  Barriers:
 //   xa_full[s]   A_g stored (the 4 dequant warps of a group) and X_g landed
 //                (TMA bytes)
 //   xa_empty[s]  the MMAs of both halves of group g completed (one commit
@@ -72,27 +74,28 @@ constexpr int THREADS = 16 * 32;
 constexpr int P_COL = 0;                  // P buffers from column 0, then the A stages
 constexpr int TMEM_COLS = 512;
 
-// BH: tokens per MMA (64 or 128); H: MMAs ("halves") per tile, so BN = BH H
+// BH: tokens per MMA (32, 64 or 128); H: MMAs ("halves") per tile, so BN = BH H
 // tokens; F8: a parent of the launch holds FP8 or NVFP4 codes (larger units,
 // so fewer weight stages fit).  Tensor memory holds the A stages and as many
-// P buffers of BH columns as fit beside them: 3 of 128 columns beside 4 A
-// stages, or 4 of 64 beside 8.  The 64-token tile's dequant is the step that
-// limits it (a unit's MMAs are short), so it gets twice the A stages, half
-// the activation stages (its X tiles are half as large) and twice the weight
-// stages, and runs four unit pairs ahead of the MMAs instead of two.
+// P buffers of BH columns as fit beside them (at most 6): 3 of 128 columns
+// beside 4 A stages, 4 of 64 or 6 of 32 beside 8.  The dequant limited the
+// 32- and 64-token tiles (a unit's MMAs are short), so they get two dequant
+// groups, twice the A stages, half the activation stages (their X tiles are
+// at most half as large) and twice the weight stages, and run four unit pairs
+// ahead of the MMAs instead of two.
 template <int BH_, int H, bool F8>
 struct Geo {
     static constexpr int BH = BH_;
     // Warps 4 .. 15: DQG groups of four dequant warps (a group decodes every
-    // DQG-th unit pair) and EW_N epilogue warps.  The 64-token tile, limited
-    // by its dequant, runs two groups beside four epilogue warps that read
-    // all 64 columns of a step; the others one group beside eight.
+    // DQG-th unit pair) and EPI_N epilogue warps.  The 32- and 64-token tiles
+    // run two groups beside four epilogue warps that read all 32 or 64
+    // columns of a step; the others one group beside eight.
     static constexpr int DQG = BH <= 64 ? 2 : 1;
     static constexpr int EPI_N = 12 - 4 * DQG;
     static constexpr int EPI_0 = DQ0 + 4 * DQG;
     static constexpr int NA = BH <= 64 ? 8 : 4;           // A stages (unit u uses u mod NA)
-    // P buffers (step j uses j mod NP): as many as fit, at most 6 (the scale
-    // ring covers NA + NP + 2 units)
+    // P buffers (step j uses j mod NP): as many as fit, at most 6 (8 or 12 on
+    // the 32-token tile measured no faster; the scale ring below bounds NP)
     static constexpr int NP = (TMEM_COLS - 32 * NA) / BH < 6 ? (TMEM_COLS - 32 * NA) / BH : 6;
     static constexpr int A_COL = P_COL + NP * BH;         // A stages: 32 columns each
     static constexpr int EW = BH / (EPI_N / 4);           // P columns per epilogue warp

@@ -51,3 +51,17 @@ def test_bench_line_on_the_gpu():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] > 0
     assert line["gpu_launches"] > 0
     assert line["clocks"]["sm_max_mhz"] > 0
+
+
+def test_kernel_code_hash_ignores_comments(tmp_path):
+    """The recorded ncu traffic stays valid across comment edits, and only those."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_module", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text("// one\nint f(int x) {  /* two */ return x + 1; }\n")
+    b.write_text("// another comment,\n// over two lines\nint f(int x) {\n    return x + 1;   // the same code\n}\n")
+    c.write_text("// one\nint f(int x) {  /* two */ return x + 2; }\n")
+    assert bench.kernel_code_sha256(str(a)) == bench.kernel_code_sha256(str(b))
+    assert bench.kernel_code_sha256(str(a)) != bench.kernel_code_sha256(str(c))

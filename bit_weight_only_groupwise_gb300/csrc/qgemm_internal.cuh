@@ -114,7 +114,7 @@ struct SkinnyArgs {
 };
 
 // The wide route covers ceil(N/128) x ceil(T/BN) output tiles per parent
-// (BN = 128 or 256 tokens).
+// (BN = 32, 64, 128 or 256 tokens).
 struct WideParent {
     const uint8_t *packed;   // units of this parent
     void *Y;                 // [T][ncols], fp32 or bf16

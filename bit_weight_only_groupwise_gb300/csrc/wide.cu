@@ -21,7 +21,9 @@
 // A tile whose groups span several CTAs is finished by the CTA that completes
 // it last: the others leave their fp32 partial sums in the workspace and
 // count in, and the last one adds them in ascending CTA order (a fixed order,
-// so results are bitwise repeatable) and writes Y.  No CTA waits for another.
+// so results are bitwise repeatable) and writes Y; the tile's first segment,
+// usually the last to finish, keeps its own partial in registers when it
+// finds the others counted in.  No CTA waits for another.
 //
 // Warp roles (16 warps; every single-issuer role is a converged warp whose
 // elected lane issues, and every wait is taken by the whole warp):
@@ -541,14 +543,16 @@ __device__ __forceinline__ void store_tile(const WideParent &P, int n, int t0, i
 __device__ __forceinline__ size_t part_q(int t, int r) { return (size_t)(t >> 2) * wide::BM + r; }
 
 // The sum of a split tile's partials, for one epilogue thread (row r, its
-// 64-token column block c of each half): every segment's partial, this CTA's
-// own included, is read back from the workspace and summed over the
-// segments' CTAs c_first .. c_last in ascending order, so the order does not
-// depend on which CTA finishes last.  acc is overwritten (its registers hold
-// the running sum, 32 column pairs of one segment in flight beside it).
+// column block c of each half), over the segments' CTAs c_first .. c_last in
+// ascending order, so the order does not depend on which CTA finishes last.
+// own: this CTA is c_first and acc still holds its segment, the first term;
+// otherwise every segment's partial, this CTA's own included, is read back
+// from the workspace and acc is overwritten.  An fp32 value read back equals
+// the one written, so both give the same bits.  (acc holds the running sum,
+// 32 column pairs of one segment in flight beside it.)
 template <int BH, int H, int NJ, int BN>
 __device__ __forceinline__ void fixup_sum(float2 (&acc)[H][NJ], const float *part, long long U, int grid,
-                                          int c_first, int c_last, long long u0, int c, int r) {
+                                          int c_first, int c_last, long long u0, int c, int r, bool own) {
     constexpr int BM = wide::BM, EW = 2 * NJ;
     constexpr int CH = H == 1 ? NJ : 16;              // column pairs in flight (registers)
 #pragma unroll
@@ -561,12 +565,14 @@ __device__ __forceinline__ void fixup_sum(float2 (&acc)[H][NJ], const float *par
                                                                    BN * BM) +
                        part_q(h * BH + EW * c + 2 * jb, r);
             };
-            const float4 *p0 = seg(c_first);
+            if (!own) {
+                const float4 *p0 = seg(c_first);
 #pragma unroll
-            for (int j = 0; j < CH; j += 2) {
-                const float4 x = __ldcg(p0 + (size_t)(j / 2) * BM);
-                acc[h][jb + j] = make_float2(x.x, x.y);
-                acc[h][jb + j + 1] = make_float2(x.z, x.w);
+                for (int j = 0; j < CH; j += 2) {
+                    const float4 x = __ldcg(p0 + (size_t)(j / 2) * BM);
+                    acc[h][jb + j] = make_float2(x.x, x.y);
+                    acc[h][jb + j + 1] = make_float2(x.z, x.w);
+                }
             }
             for (int cc = c_first + 1; cc <= c_last; ++cc) {
                 const float4 *pc = seg(cc);
@@ -822,24 +828,41 @@ __global__ void __launch_bounds__(wide::THREADS, 1)
             } else {
                 const long long u0 = (long long)tile * G;
                 const int c_first = range_cta(U, gridDim.x, u0), c_last = range_cta(U, gridDim.x, u0 + G - 1);
-                // a CTA's first segment goes to its slot 0, its last to slot 1
-                float4 *mine = reinterpret_cast<float4 *>(args.part + (size_t)(blockIdx.x * 2 + (lo >= u0 ? 0 : 1)) * BN * BM);
-#pragma unroll
-                for (int h = 0; h < H; ++h)
-#pragma unroll
-                    for (int j = 0; j < NJ; j += 2)
-                        mine[part_q(h * BH + EW * c + 2 * j, r)] =
-                            make_float4(acc[h][j].x, acc[h][j].y, acc[h][j + 1].x, acc[h][j + 1].y);
-                __threadfence();
-                __syncwarp();
+                const unsigned int others = (unsigned int)(c_last - c_first);
                 unsigned int *cnt = tr.P->cnt + (size_t)tr.local * EPI_WARPS + e;
-                unsigned int old = 0;
-                if (lane == 0) old = atomicAdd(cnt, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned int)(c_last - c_first)) {
-                    // the last of the tile's segments sums them all
+                // The head segment (the tile's first groups) closes its CTA's
+                // range while the tile's other segments open theirs, so it
+                // usually finishes last.  If every other segment has counted
+                // in, it sums from its registers and writes no partial: the
+                // counter then never reaches the count that would make
+                // another segment the summing one.
+                bool own = false;
+                if ((int)blockIdx.x == c_first) {
+                    unsigned int seen = 0;
+                    if (lane == 0) seen = ld_acquire_gpu(cnt);
+                    own = __shfl_sync(0xffffffffu, seen, 0) == others;
+                }
+                bool sum = own;
+                if (!own) {
+                    // a CTA's first segment goes to its slot 0, its last to slot 1
+                    float4 *mine =
+                        reinterpret_cast<float4 *>(args.part + (size_t)(blockIdx.x * 2 + (lo >= u0 ? 0 : 1)) * BN * BM);
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+#pragma unroll
+                        for (int j = 0; j < NJ; j += 2)
+                            mine[part_q(h * BH + EW * c + 2 * j, r)] =
+                                make_float4(acc[h][j].x, acc[h][j].y, acc[h][j + 1].x, acc[h][j + 1].y);
                     __threadfence();
-                    fixup_sum<BH, H, NJ, BN>(acc, args.part, U, (int)gridDim.x, c_first, c_last, u0, c, r);
+                    __syncwarp();
+                    unsigned int old = 0;
+                    if (lane == 0) old = atomicAdd(cnt, 1u);
+                    sum = __shfl_sync(0xffffffffu, old, 0) == others;
+                    if (sum) __threadfence();
+                }
+                if (sum) {
+                    // the last of the tile's segments sums them all
+                    fixup_sum<BH, H, NJ, BN>(acc, args.part, U, (int)gridDim.x, c_first, c_last, u0, c, r, own);
                     if (lane == 0) *cnt = 0;              // zero again for the next run
                     store_tile<BH, H, NJ, FUSED>(*tr.P, n, t0, T, acc);
                 }
